@@ -1,0 +1,102 @@
+"""The ring KV cache and its three calls, as plain definitions.
+
+Runway Characters paper:
+* §4.1 "A ring cache with a device-side write position": one allocation per
+  cache; each new chunk goes into circular slots; the write position advances
+  with every write.  Each cached token keeps the position it was written with.
+* §4.2 "RoPE at write, and a delta rotation at reset": RoPE is applied to the
+  new tokens' keys once, before the write; at a reset every cached key is
+  dequantised, rotated by R(-d) on the temporal frequencies in fp32 and
+  re-quantised; values are not touched (Appendix G).
+* §4.3 "FP8 at write": K and V are stored as e4m3; queries are quantised per
+  call.
+* Appendix G: every attention call reads all the cache's slots.
+
+State: codes uint8 [H, S, D] for K and V, fp32 scales [H, S], the write
+position ``wp`` and the count of valid slots ``n_valid``.  A write of N tokens
+puts token i into slot (wp + i) mod S, then wp <- (wp + N) mod S and
+n_valid <- min(n_valid + N, S).  Slots fill in order 0, 1, 2, ... so the valid
+slots are always 0 .. n_valid-1; attention is a sum over them and does not
+depend on their order.
+
+Scales are per (token, head), recomputed at write and at reset (absmax, see
+``quant``); this replaces the paper's per-(layer, head) scales calibrated once
+per session.
+"""
+import numpy as np
+
+from . import quant, rope
+from .attention import attend_f64
+
+
+class OracleRing:
+    def __init__(self, heads, head_dim, n_slots, axis_dims, base=10000.0):
+        if sum(axis_dims) != head_dim or any(d % 2 for d in axis_dims):
+            raise ValueError("axis_dims must be even and sum to head_dim")
+        self.H, self.D, self.S = int(heads), int(head_dim), int(n_slots)
+        self.axis_dims = tuple(int(d) for d in axis_dims)
+        self.base = float(base)
+        self.k_codes = np.zeros((self.H, self.S, self.D), np.uint8)
+        self.v_codes = np.zeros((self.H, self.S, self.D), np.uint8)
+        self.k_scale = np.zeros((self.H, self.S), np.float32)
+        self.v_scale = np.zeros((self.H, self.S), np.float32)
+        self.wp = 0
+        self.n_valid = 0
+
+    # -- write ---------------------------------------------------------------
+    def slots_for(self, n_new):
+        return (self.wp + np.arange(n_new)) % self.S
+
+    def write(self, k, v, pos):
+        """k, v: float32 [N, H, D] (bf16 values); pos: int [N, n_axes].
+        Returns the slot index of each token."""
+        k = np.asarray(k, np.float32)
+        v = np.asarray(v, np.float32)
+        n = k.shape[0]
+        if not 1 <= n <= self.S:
+            raise ValueError("a write must carry 1 .. n_slots tokens")
+        kc, ks = quant.quantize_rows(rope.rope_f32(k, pos, self.axis_dims, self.base))
+        vc, vs = quant.quantize_rows(v)
+        slots = self.slots_for(n)
+        self.k_codes[:, slots, :] = np.transpose(kc, (1, 0, 2))
+        self.v_codes[:, slots, :] = np.transpose(vc, (1, 0, 2))
+        self.k_scale[:, slots] = ks.T
+        self.v_scale[:, slots] = vs.T
+        self.wp = int((self.wp + n) % self.S)
+        self.n_valid = int(min(self.n_valid + n, self.S))
+        return slots
+
+    # -- reset ---------------------------------------------------------------
+    def reset_positions(self, d):
+        """Rotate every valid cached key by R(-d) on the temporal axis
+        (axis 0), in fp32, and re-quantise it with a fresh absmax scale."""
+        n = self.n_valid
+        if n == 0:
+            return
+        c, s = rope.delta_cos_sin_f32(d, self.axis_dims[0], self.base)
+        k = quant.dequantize_rows(self.k_codes[:, :n], self.k_scale[:, :n])
+        k = rope.rotate_temporal_f32(k, c, s, self.axis_dims[0])
+        codes, scale = quant.quantize_rows(k)
+        self.k_codes[:, :n] = codes
+        self.k_scale[:, :n] = scale
+
+    # -- attend --------------------------------------------------------------
+    def quantized_queries(self, q, q_pos):
+        """RoPE (fp32) then per-token-per-head e4m3: (codes [Nq,H,D], scale [Nq,H])."""
+        return quant.quantize_rows(rope.rope_f32(np.asarray(q, np.float32), q_pos,
+                                                 self.axis_dims, self.base))
+
+    def attend(self, q, q_pos, heads=None, rows=None):
+        """fp64 attention of the quantised queries over the valid slots.
+
+        q: float32 [Nq, H, D] (bf16 values); q_pos: int [Nq, n_axes].
+        ``heads`` / ``rows`` restrict the output to some heads / query rows
+        (for sampled checks); the result is [len(rows), len(heads), D]."""
+        qc, qs = self.quantized_queries(q, q_pos)
+        heads = np.arange(self.H) if heads is None else np.asarray(heads)
+        rows = np.arange(qc.shape[0]) if rows is None else np.asarray(rows)
+        qh = quant.dequantize_rows_f64(qc[rows][:, heads], qs[rows][:, heads])
+        n = self.n_valid
+        kh = quant.dequantize_rows_f64(self.k_codes[heads, :n], self.k_scale[heads, :n])
+        vh = quant.dequantize_rows_f64(self.v_codes[heads, :n], self.v_scale[heads, :n])
+        return attend_f64(qh, kh, vh)

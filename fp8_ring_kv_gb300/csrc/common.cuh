@@ -1,0 +1,113 @@
+// Internal definitions shared by the kvring kernels and the host launcher.
+#pragma once
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "sm103_ptx.cuh"
+
+namespace kvring_dev {
+
+constexpr int kMaxAxes = 3;
+constexpr float kE4m3Max = 448.0f;
+
+// state words at the start of the workspace
+enum : int { ST_WP = 0, ST_NVALID = 1, ST_ERR = 2, ST_DONE = 3, ST_WORDS = 64 };
+enum : int { DEVERR_POS_RANGE = 1, DEVERR_EMPTY = 2, DEVERR_TIMEOUT = 4 };
+
+// Device view of one ring, passed by value to every kernel.
+struct RingView {
+  int32_t* state;                 // ST_* words
+  const float2* rope[kMaxAxes];   // per axis: [pos_count][axis_dims/2] (cos, sin)
+  int32_t pos_min[kMaxAxes];
+  int32_t pos_count[kMaxAxes];
+  int32_t axis_pairs[kMaxAxes];   // axis_dims / 2
+  int32_t pair_off[kMaxAxes];     // index of the first pair of each axis
+  uint8_t* k_codes;               // [H][S][D]
+  uint8_t* v_codes;               // [H][S][D]
+  float* k_scale;                 // [H][S_pad]
+  float* v_scale;                 // [H][S_pad]
+  int32_t H, D, S, S_pad, n_axes;
+};
+
+// ---------------------------------------------------------------- numerics
+// These are the exact fp32 operation sequences the method fixes; the compiler
+// must not contract or reorder them (no fast-math, explicit _rn intrinsics).
+
+// One RoPE pair: (x0 c - x1 s, x0 s + x1 c), every product and sum rounded.
+__device__ __forceinline__ void rope_pair(float& x0, float& x1, float c, float s) {
+  const float a = __fsub_rn(__fmul_rn(x0, c), __fmul_rn(x1, s));
+  const float b = __fadd_rn(__fmul_rn(x0, s), __fmul_rn(x1, c));
+  x0 = a;
+  x1 = b;
+}
+
+// Scale and its inverse for a row whose absolute maximum is ``amax``:
+// scale = amax / 448, inv = 448 / amax, both IEEE-rounded; zero rows get 0.
+__device__ __forceinline__ void absmax_scale(float amax, float& scale, float& inv) {
+  if (amax > 0.0f) {
+    scale = __fdiv_rn(amax, kE4m3Max);
+    inv = __fdiv_rn(kE4m3Max, amax);
+  } else {
+    scale = 0.0f;
+    inv = 0.0f;
+  }
+}
+
+// 16 values -> 16 e4m3 codes (round to nearest even, saturating) of x * inv.
+// A zero row (inv == 0) gives all-zero codes (+0).
+__device__ __forceinline__ uint4 quant16(const float* x, float inv) {
+  uint32_t w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t lo = cvt_e4m3x2(__fmul_rn(x[4 * i + 0], inv), __fmul_rn(x[4 * i + 1], inv));
+    const uint32_t hi = cvt_e4m3x2(__fmul_rn(x[4 * i + 2], inv), __fmul_rn(x[4 * i + 3], inv));
+    w[i] = lo | (hi << 16);
+  }
+  if (inv == 0.0f) w[0] = w[1] = w[2] = w[3] = 0u;
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// 16 e4m3 codes -> 16 fp32 values (exact).
+__device__ __forceinline__ void dequant16_codes(uint4 c, float* x) {
+  const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t lo = cvt_e4m3x2_to_f16x2((uint16_t)(w[i] & 0xFFFFu));
+    const uint32_t hi = cvt_e4m3x2_to_f16x2((uint16_t)(w[i] >> 16));
+    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&lo));
+    const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&hi));
+    x[4 * i + 0] = a.x;
+    x[4 * i + 1] = a.y;
+    x[4 * i + 2] = b.x;
+    x[4 * i + 3] = b.y;
+  }
+}
+
+// 8 bf16 (one uint4) -> 8 fp32 (exact).
+__device__ __forceinline__ void bf16x8_to_f32(uint4 u, float* x) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    x[2 * i + 0] = __uint_as_float(w[i] << 16);
+    x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+// The axis and in-axis index of RoPE pair p, and its table entry for the
+// given positions.  Out-of-range positions are clamped and flagged.
+__device__ __forceinline__ float2 rope_cs(const RingView& rv, const int32_t* pos_row, int p, bool& bad) {
+  int a = 0;
+  if (rv.n_axes > 1 && p >= rv.pair_off[1]) a = 1;
+  if (rv.n_axes > 2 && p >= rv.pair_off[2]) a = 2;
+  const int j = p - rv.pair_off[a];
+  int idx = pos_row[a] - rv.pos_min[a];
+  if (idx < 0 || idx >= rv.pos_count[a]) {
+    bad = true;
+    idx = idx < 0 ? 0 : rv.pos_count[a] - 1;
+  }
+  return __ldg(rv.rope[a] + (size_t)idx * rv.axis_pairs[a] + j);
+}
+
+}  // namespace kvring_dev

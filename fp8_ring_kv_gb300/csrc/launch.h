@@ -1,0 +1,33 @@
+// Host-side entry points of the kernels (internal to libkvring).
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+namespace kvring_dev {
+
+// cos/sin of the reset rotation -d * omega_{0,j} for the temporal pairs j,
+// formed in fp64 on the host and rounded once to fp32.
+struct DeltaTable {
+  float2 cs[64];
+  int n_pairs;
+};
+
+struct AttnMaps {
+  CUtensorMap k_codes;   // [H][S][D] u8, box {D, 128, 1}
+  CUtensorMap v_codes;
+  CUtensorMap k_scale;   // [H][S_pad] f32, box {128, 1}
+  CUtensorMap v_scale;
+};
+
+cudaError_t launch_ring_kv_write(const RingView& rv, const void* k, const void* v, const int32_t* pos, int n_new,
+                                 cudaStream_t st);
+cudaError_t launch_delta_rerotate(const RingView& rv, const DeltaTable& dt, cudaStream_t st);
+cudaError_t launch_debug_quantize(const float* x, long long rows, int d, uint8_t* codes, float* scales,
+                                  cudaStream_t st);
+cudaError_t prepare_attend(int D);   // once per device: opt in to the kernel's shared memory
+cudaError_t launch_fp8_ring_attn(const RingView& rv, const AttnMaps& maps, const void* q, const int32_t* q_pos,
+                                 int n_q, void* out, int out_f32, cudaStream_t st);
+
+}  // namespace kvring_dev

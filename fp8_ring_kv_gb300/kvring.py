@@ -1,0 +1,222 @@
+"""ctypes binding of libkvring (include/kvring.h).
+
+Argument marshalling only: every step of the path runs in the library's CUDA
+kernels.  PyTorch provides device memory (the workspace and the I/O tensors)
+and streams.  The library must be built (``fp8_ring_kv_gb300.build``); if it
+is missing, loading fails loudly -- there is no other implementation.
+"""
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libkvring.so")
+
+KVRING_OK = 0
+KVRING_ERR_INVALID_ARG = -1
+KVRING_ERR_MISALIGNED = -2
+KVRING_ERR_UNSUPPORTED = -3
+KVRING_ERR_CUDA = -4
+KVRING_ERR_WORKSPACE = -5
+KVRING_ERR_NO_DEVICE = -6
+
+KVRING_DEVERR_POS_RANGE = 1
+KVRING_DEVERR_EMPTY = 2
+KVRING_DEVERR_TIMEOUT = 4
+
+KVRING_OUT_BF16 = 0
+KVRING_OUT_F32 = 1
+
+EXPORTS = (
+    "kvring_workspace_bytes", "kvring_create", "kvring_write", "kvring_reset_positions",
+    "kvring_attend", "kvring_destroy", "kvring_status_string", "kvring_last_cuda_error",
+    "kvring_layout", "kvring_debug_state", "kvring_debug_quantize",
+)
+
+
+class kvring_config(ctypes.Structure):
+    _fields_ = [
+        ("heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32),
+        ("n_slots", ctypes.c_int32),
+        ("n_axes", ctypes.c_int32),
+        ("axis_dims", ctypes.c_int32 * 3),
+        ("pos_min", ctypes.c_int32 * 3),
+        ("pos_count", ctypes.c_int32 * 3),
+        ("rope_base", ctypes.c_double),
+        ("out_dtype", ctypes.c_int32),
+    ]
+
+
+class KVRingError(RuntimeError):
+    pass
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libkvring.so (once) and declare its signatures."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise ImportError(f"libkvring is not built ({path} missing): run fp8_ring_kv_gb300.build.build()")
+    lib = ctypes.CDLL(path)
+    vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+    cfgp = ctypes.POINTER(kvring_config)
+    sig = {
+        "kvring_workspace_bytes": (sz, [cfgp]),
+        "kvring_create": (ctypes.c_int, [cfgp, vp, sz, vp, ctypes.POINTER(vp)]),
+        "kvring_write": (ctypes.c_int, [vp, vp, vp, vp, i32, vp]),
+        "kvring_reset_positions": (ctypes.c_int, [vp, i32, vp]),
+        "kvring_attend": (ctypes.c_int, [vp, vp, vp, i32, vp, vp]),
+        "kvring_destroy": (ctypes.c_int, [vp]),
+        "kvring_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+        "kvring_last_cuda_error": (ctypes.c_int, []),
+        "kvring_layout": (ctypes.c_int, [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), ctypes.POINTER(vp),
+                                         ctypes.POINTER(vp), ctypes.POINTER(vp), ctypes.POINTER(i32)]),
+        "kvring_debug_state": (ctypes.c_int, [vp, vp, ctypes.POINTER(i32)]),
+        "kvring_debug_quantize": (ctypes.c_int, [vp, i64, i32, vp, vp, vp]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def check(status: int, what: str = "") -> None:
+    if status != KVRING_OK:
+        lib = load()
+        msg = lib.kvring_status_string(status).decode()
+        if status == KVRING_ERR_CUDA:
+            msg += f" (cudaError {lib.kvring_last_cuda_error()})"
+        raise KVRingError(f"{what}: {msg} [{status}]")
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _ptr(t) -> ctypes.c_void_p:
+    return ctypes.c_void_p(t if isinstance(t, int) else t.data_ptr())
+
+
+def make_config(heads, head_dim, n_slots, axis_dims, pos_min, pos_count, rope_base=10000.0,
+                out_dtype=KVRING_OUT_F32) -> kvring_config:
+    c = kvring_config()
+    c.heads, c.head_dim, c.n_slots = int(heads), int(head_dim), int(n_slots)
+    c.n_axes = len(axis_dims)
+    for a in range(3):
+        c.axis_dims[a] = int(axis_dims[a]) if a < len(axis_dims) else 0
+        c.pos_min[a] = int(pos_min[a]) if a < len(axis_dims) else 0
+        c.pos_count[a] = int(pos_count[a]) if a < len(axis_dims) else 0
+    c.rope_base = float(rope_base)
+    c.out_dtype = int(out_dtype)
+    return c
+
+
+# --- the C-ABI calls under their own names ----------------------------------
+def kvring_workspace_bytes(cfg: kvring_config) -> int:
+    return int(load().kvring_workspace_bytes(ctypes.byref(cfg)))
+
+
+def kvring_create(cfg: kvring_config, workspace: torch.Tensor, stream=None) -> ctypes.c_void_p:
+    h = ctypes.c_void_p()
+    check(load().kvring_create(ctypes.byref(cfg), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                               _stream(stream), ctypes.byref(h)), "kvring_create")
+    return h
+
+
+def kvring_write(handle, k, v, pos, n_new: int, stream=None) -> None:
+    check(load().kvring_write(handle, _ptr(k), _ptr(v), _ptr(pos), int(n_new), _stream(stream)), "kvring_write")
+
+
+def kvring_reset_positions(handle, d: int, stream=None) -> None:
+    check(load().kvring_reset_positions(handle, int(d), _stream(stream)), "kvring_reset_positions")
+
+
+def kvring_attend(handle, q, q_pos, n_q: int, out, stream=None) -> None:
+    check(load().kvring_attend(handle, _ptr(q), _ptr(q_pos), int(n_q), _ptr(out), _stream(stream)),
+          "kvring_attend")
+
+
+def kvring_destroy(handle) -> None:
+    check(load().kvring_destroy(handle), "kvring_destroy")
+
+
+def kvring_debug_quantize(x, rows: int, d: int, codes, scales, stream=None) -> None:
+    check(load().kvring_debug_quantize(_ptr(x), int(rows), int(d), _ptr(codes), _ptr(scales), _stream(stream)),
+          "kvring_debug_quantize")
+
+
+# --- a convenience object over one ring ----------------------------------------
+class KVRing:
+    """One ring in a torch-allocated device workspace.
+
+    ``write``/``reset_positions``/``attend`` enqueue the library's kernels on
+    the current (or given) stream and return at once."""
+
+    def __init__(self, heads, head_dim, n_slots, axis_dims, pos_min, pos_count, rope_base=10000.0,
+                 out_dtype=KVRING_OUT_F32, device="cuda", stream=None):
+        self.cfg = make_config(heads, head_dim, n_slots, axis_dims, pos_min, pos_count, rope_base, out_dtype)
+        nbytes = kvring_workspace_bytes(self.cfg)
+        if nbytes == 0:
+            raise KVRingError("invalid kvring configuration")
+        self.heads, self.head_dim, self.n_slots = int(heads), int(head_dim), int(n_slots)
+        self.n_axes = len(axis_dims)
+        self.out_dtype = torch.float32 if out_dtype == KVRING_OUT_F32 else torch.bfloat16
+        self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        self.handle = kvring_create(self.cfg, self.workspace, stream)
+        ptrs = [ctypes.c_void_p() for _ in range(5)]
+        s_pad = ctypes.c_int32()
+        check(load().kvring_layout(self.handle, *[ctypes.byref(p) for p in ptrs], ctypes.byref(s_pad)),
+              "kvring_layout")
+        self.s_pad = int(s_pad.value)
+        base = self.workspace.data_ptr()
+        off = [p.value - base for p in ptrs]
+        H, S, D = self.heads, self.n_slots, self.head_dim
+        ws = self.workspace
+        self.k_codes = ws[off[0]:off[0] + H * S * D].view(H, S, D)
+        self.v_codes = ws[off[1]:off[1] + H * S * D].view(H, S, D)
+        self.k_scales = ws[off[2]:off[2] + H * self.s_pad * 4].view(torch.float32).view(H, self.s_pad)
+        self.v_scales = ws[off[3]:off[3] + H * self.s_pad * 4].view(torch.float32).view(H, self.s_pad)
+        self.state_words = ws[off[4]:off[4] + 16].view(torch.int32)
+
+    @classmethod
+    def from_shape(cls, shape, out_dtype=KVRING_OUT_F32, device="cuda", stream=None):
+        return cls(shape.heads, shape.head_dim, shape.n_slots, shape.axis_dims, shape.pos_min, shape.pos_count,
+                   shape.rope_base, out_dtype, device, stream)
+
+    def write(self, k, v, pos, stream=None):
+        kvring_write(self.handle, k, v, pos, k.shape[0], stream)
+
+    def reset_positions(self, d, stream=None):
+        kvring_reset_positions(self.handle, d, stream)
+
+    def attend(self, q, q_pos, out=None, stream=None):
+        if out is None:
+            out = torch.empty(q.shape, dtype=self.out_dtype, device=q.device)
+        kvring_attend(self.handle, q, q_pos, q.shape[0], out, stream)
+        return out
+
+    def debug_state(self, stream=None):
+        arr = (ctypes.c_int32 * 3)()
+        check(load().kvring_debug_state(self.handle, _stream(stream), arr), "kvring_debug_state")
+        return int(arr[0]), int(arr[1]), int(arr[2])
+
+    def close(self):
+        if self.handle is not None:
+            kvring_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

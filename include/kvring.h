@@ -1,0 +1,200 @@
+/*
+ * kvring — a write-time FP8 ring KV cache for one GPU (sm_103a) and the
+ * attention that reads it.
+ *
+ * Source: "Runway Characters: Serving a 57B Video Diffusion Transformer for
+ * Real-Time Conversation" (arXiv:2611.05642):
+ *   §4.1  a ring cache with a device-side write position;
+ *   §4.2  RoPE applied once at write, and a delta rotation of the cached keys
+ *         when positions reset;
+ *   §4.3  K and V stored as float8_e4m3, queries quantised per call;
+ *   App. G  cache update and position reset; every attention call reads all
+ *         valid slots of its cache.
+ *
+ * Every call is asynchronous on the caller's CUDA stream, moves no data
+ * between host and device (except the two documented debug calls), and can
+ * be captured in a CUDA graph: the write position lives in device memory and
+ * is advanced by the write kernel itself.
+ *
+ * Memory: the caller owns all device memory.  kvring_create carves one
+ * caller-allocated device workspace (kvring_workspace_bytes bytes, 256-byte
+ * aligned) into the ring state, the RoPE tables, the e4m3 code arrays and the
+ * scale arrays.  The handle itself owns host memory only; kvring_destroy
+ * frees that and nothing else.
+ *
+ * Numbers and layouts:
+ *   H = heads, D = head_dim, S = n_slots.
+ *   bf16 inputs are row-major [n][H][D]; positions are int32 [n][n_axes].
+ *   K codes and V codes are e4m3 [H][S][D]; K and V scales are fp32
+ *   [H][S_pad] (S_pad = S rounded up to a multiple of 4); a (token, head)
+ *   row's dequantised value is code * scale.
+ *
+ * Errors: every call returns KVRING_OK (0) or a negative status; arguments
+ * are checked on the host before anything is enqueued.  Conditions only the
+ * GPU can see (a position outside the RoPE table, attention over an empty
+ * ring, a wait that exceeded its time limit) set bits in a device-side error
+ * word that kvring_debug_state reads; the kernels never trap.  Non-finite
+ * inputs are undefined behaviour.  A handle must not be used by two host
+ * threads at once.
+ */
+#ifndef KVRING_H
+#define KVRING_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct kvring kvring;           /* opaque host handle */
+typedef struct CUstream_st* kvring_stream; /* a cudaStream_t; NULL = legacy default stream */
+
+enum {
+  KVRING_OK = 0,
+  KVRING_ERR_INVALID_ARG = -1,  /* null pointer, bad size or configuration */
+  KVRING_ERR_MISALIGNED = -2,   /* a pointer is not aligned as required */
+  KVRING_ERR_UNSUPPORTED = -3,  /* shape outside the kernels' set (see kvring_config) */
+  KVRING_ERR_CUDA = -4,         /* a CUDA runtime/driver call failed; kvring_last_cuda_error says which */
+  KVRING_ERR_WORKSPACE = -5,    /* workspace too small */
+  KVRING_ERR_NO_DEVICE = -6     /* no sm_100-family GPU is current */
+};
+
+/* bits of the device-side error word */
+enum {
+  KVRING_DEVERR_POS_RANGE = 1,  /* a position fell outside its axis's RoPE table (clamped) */
+  KVRING_DEVERR_EMPTY = 2,      /* attention over a ring with no valid slot (output zeros) */
+  KVRING_DEVERR_TIMEOUT = 4     /* a kernel gave up on a wait after its time limit */
+};
+
+enum { KVRING_OUT_BF16 = 0, KVRING_OUT_F32 = 1 };
+
+/*
+ * Cache geometry and RoPE layout.
+ *   heads      1 .. 128
+ *   head_dim   64 or 128
+ *   n_slots    1 .. 1<<20 ring slots
+ *   n_axes     1 .. 3 RoPE axes; axis 0 is the temporal axis (the one the
+ *              delta rotation of kvring_reset_positions turns)
+ *   axis_dims  channels per axis, each even, summing to head_dim; axis a
+ *              covers channels [o_a, o_a + axis_dims[a]) with o_a the sum of
+ *              the earlier axes, and its pair j is channels (o_a+2j, o_a+2j+1)
+ *   pos_min, pos_count
+ *              the RoPE table of axis a covers integer positions
+ *              pos_min[a] .. pos_min[a] + pos_count[a] - 1 (pos_count >= 1);
+ *              positions outside it are clamped and flagged
+ *              (KVRING_DEVERR_POS_RANGE)
+ *   rope_base  the frequency base: omega_{a,j} = rope_base^(-2j/axis_dims[a])
+ *   out_dtype  KVRING_OUT_BF16 or KVRING_OUT_F32 for kvring_attend's output
+ */
+typedef struct {
+  int32_t heads;
+  int32_t head_dim;
+  int32_t n_slots;
+  int32_t n_axes;
+  int32_t axis_dims[3];
+  int32_t pos_min[3];
+  int32_t pos_count[3];
+  double rope_base;
+  int32_t out_dtype;
+} kvring_config;
+
+/* Bytes of device workspace kvring_create needs for this configuration
+ * (0 if the configuration is invalid). */
+size_t kvring_workspace_bytes(const kvring_config* cfg);
+
+/*
+ * Create a ring in the caller's device workspace (device pointer, 256-byte
+ * aligned, at least kvring_workspace_bytes).  Enqueued on ``stream``: zeroes
+ * the ring state (write position 0, no valid slot, error word 0) and the code
+ * and scale arrays, and uploads the fp32 RoPE tables (cos and sin of
+ * pos * omega_{a,j}, formed in fp64 and rounded once).  The workspace must
+ * stay allocated until kvring_destroy.  Paper §4.1 (one allocation per cache,
+ * device-side write position).
+ */
+int kvring_create(const kvring_config* cfg, void* workspace, size_t workspace_bytes, kvring_stream stream,
+                  kvring** out);
+
+/*
+ * Write n_new tokens (ring_kv_write).  Paper §4.2 (RoPE at write), §4.3 (FP8
+ * at write), §4.1 (ring slot at the device-side write position).
+ *   k, v   device bf16 [n_new][H][D], 16-byte aligned; not modified
+ *   pos    device int32 [n_new][n_axes], 4-byte aligned
+ *   n_new  1 .. n_slots
+ * For token i and head h: K is rotated by RoPE at pos[i] in fp32, V is not;
+ * each (token, head) row of K and of V gets one fp32 scale amax/448 and e4m3
+ * codes round-to-nearest-even(x * (448/amax)) saturated to +-448; they go to
+ * slot (wp + i) mod S, where wp is the device-side write position.  Then, on
+ * the device, wp <- (wp + n_new) mod S and n_valid <- min(n_valid + n_new, S).
+ */
+int kvring_write(kvring* r, const void* k, const void* v, const int32_t* pos, int32_t n_new,
+                 kvring_stream stream);
+
+/*
+ * Position reset by d (delta_rerotate).  Paper §4.2 and App. G: every cached
+ * key moves from temporal position p to p - d; with RoPE angles affine in the
+ * position, that is one rotation R(-d * omega_{0,j}) of each temporal-axis
+ * pair.  Every valid key row is dequantised (code * scale, fp32), its
+ * temporal pairs are rotated in fp32 by the fp32-rounded cos/sin of
+ * -d * omega_{0,j} (formed in fp64 on the host), and the row is re-quantised
+ * with a fresh absmax scale, in place.  Values are not touched.  ``d`` is a
+ * host value and is baked into a captured graph.  Callers pass positions
+ * shifted by -d to later calls; the library keeps no position counter.
+ */
+int kvring_reset_positions(kvring* r, int32_t d, kvring_stream stream);
+
+/*
+ * Attention of n_q queries over every valid slot (fp8_ring_attn).  Paper §4.3
+ * (queries quantised per call; attention reads the FP8 cache with per-token
+ * scales) and App. G (all slots read).
+ *   q      device bf16 [n_q][H][D], 16-byte aligned
+ *   q_pos  device int32 [n_q][n_axes]
+ *   n_q    >= 1
+ *   out    device [n_q][H][D], bf16 or fp32 as configured, 16-byte aligned
+ * Each query row is rotated by RoPE at q_pos (fp32) and quantised to e4m3
+ * with its own scale; out = softmax(q.k / sqrt(D)) v over slots
+ * 0 .. n_valid-1 with dequantised q, k and v, no mask.  Scores come from FP8
+ * tensor-core products with fp32 accumulation; the softmax weights are
+ * rounded to fp16 for the weighted sum of V.
+ */
+int kvring_attend(kvring* r, const void* q, const int32_t* q_pos, int32_t n_q, void* out,
+                  kvring_stream stream);
+
+/* Free the host handle (the workspace stays the caller's). NULL is allowed. */
+int kvring_destroy(kvring* r);
+
+/* Static description of a status code. */
+const char* kvring_status_string(int status);
+
+/* The last cudaError_t value seen by a call that returned KVRING_ERR_CUDA
+ * on this host thread. */
+int kvring_last_cuda_error(void);
+
+/*
+ * Device pointers into the workspace, for inspection (tests, tools):
+ * K codes, V codes, K scales, V scales, the int32 state word array
+ * {wp, n_valid, error, internal}, and S_pad.  Any out pointer may be NULL.
+ */
+int kvring_layout(const kvring* r, void** k_codes, void** v_codes, void** k_scales, void** v_scales,
+                  void** state, int32_t* s_pad);
+
+/*
+ * DEBUG, SYNCHRONISING: wait for ``stream`` and copy the device state to
+ * out3 = {wp, n_valid, error bits}.  Not for the hot path (it is the one
+ * host<->device read the library offers).
+ */
+int kvring_debug_state(const kvring* r, kvring_stream stream, int32_t* out3);
+
+/*
+ * The quantiser of ring_kv_write applied to raw fp32 rows, for checking the
+ * e4m3 cast bit for bit: x device fp32 [rows][d] (16-byte aligned, d a
+ * multiple of 16, 16 .. 256) -> codes device u8 [rows][d], scales device fp32
+ * [rows].  Asynchronous on ``stream``.
+ */
+int kvring_debug_quantize(const float* x, int64_t rows, int32_t d, uint8_t* codes, float* scales,
+                          kvring_stream stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KVRING_H */

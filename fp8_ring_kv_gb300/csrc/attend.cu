@@ -10,14 +10,16 @@
 //
 //   S_j  = Qcodes . Kcodes_j^T            tcgen05 kind::f8f6f4, fp32 in TMEM
 //   t    = S_j * s_k (per column);  logit*log2(e) = t * s_q * log2(e)/sqrt(D)
-//   online softmax in base 2 (running max m, running sum l of exp2(t - m))
-//   P'   = exp2(.) * s_v * C_v  rounded to fp16  (s_v per slot = per column)
-//   O   += P' . Vcodes_j                   tcgen05 kind::f16, fp32 in TMEM
-//   out  = O / (l * C_v)
+//   online softmax in base 2: e = exp2(t*r - m + c), l += e, with a running
+//   row maximum m that is only raised (and O rescaled) when a tile's maximum
+//   exceeds it by more than 2^8, so e <= 2^8 * 2^c
+//   P    = e * s_v (per column) rounded to fp16, stored to TMEM
+//   O   += P . Vcodes_j                    tcgen05 kind::f16 (A = P from TMEM)
+//   out  = O / l
 // The e4m3 V codes are widened to fp16 in shared memory (exact) because the
 // fp16 MMA takes both operands in fp16; P in fp16 keeps the weighted sum of V
-// within the accuracy the e4m3 weights would lose.  C_v is a per-head power
-// of two that keeps P' within fp16 range.
+// within the accuracy that e4m3 weights would lose.  2^c is a per-head power of
+// two (cancelling between O and l) that keeps P within fp16 range.
 //
 // Warp roles (320 threads):
 //   warps 0-3  softmax + epilogue, thread r owns query row r (TMEM lane r)
@@ -37,8 +39,10 @@ constexpr int BN = 128;           // slots per tile
 constexpr int NSTAGE = 2;         // fp8 K/V stages
 constexpr int ATT_THREADS = 320;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t TM_S = 0;      // two S buffers at columns 0 and 128
-constexpr uint32_t TM_O = 256;    // O accumulator
+constexpr uint32_t TM_S = 0;      // two fp32 S buffers at columns 0 and 128
+constexpr uint32_t TM_P = 256;    // two fp16 P buffers (64 columns each) at 256 and 320
+constexpr uint32_t TM_O = 384;    // fp32 O accumulator (D columns)
+constexpr float kLazyRescale = 8.0f;   // log2 of the largest unnormalised weight
 
 template <int D>
 struct AttnLayout {
@@ -46,8 +50,7 @@ struct AttnLayout {
   static constexpr int K0 = Q + BM * D;                  // NSTAGE x e4m3 [BN][D]
   static constexpr int V0 = K0 + NSTAGE * BN * D;        // NSTAGE x e4m3 [BN][D]
   static constexpr int VH0 = V0 + NSTAGE * BN * D;       // 2 x fp16 [BN][D], MN-major swizzled
-  static constexpr int P0 = VH0 + 2 * BN * D * 2;        // 2 x fp16 [BM][BN], K-major swizzled
-  static constexpr int SK0 = P0 + 2 * BM * BN * 2;       // NSTAGE x fp32 [BN]
+  static constexpr int SK0 = VH0 + 2 * BN * D * 2;       // NSTAGE x fp32 [BN]
   static constexpr int SV0 = SK0 + NSTAGE * BN * 4;
   static constexpr int SQ = SV0 + NSTAGE * BN * 4;       // fp32 [BM]
   static constexpr int BAR = SQ + BM * 4;
@@ -56,12 +59,6 @@ struct AttnLayout {
   static constexpr int BYTES = MISC + 64;
   static constexpr int ALLOC = BYTES + 1024;             // slack for 1024-byte alignment
 };
-
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
 
 // byte offset of 16-byte chunk c of row r in a K-major tile whose rows are
 // D bytes (D = 128: 128-byte swizzle; D = 64: 64-byte swizzle)
@@ -102,7 +99,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + LY::MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + LY::MISC + 4);
   int* maxsv_bits = reinterpret_cast<int*>(sm + LY::MISC + 8);
-  float* cv_smem = reinterpret_cast<float*>(sm + LY::MISC + 12);
+  float* cv_smem = reinterpret_cast<float*>(sm + LY::MISC + 12);   // log2 of the per-head weight factor
   float* sq_smem = reinterpret_cast<float*>(sm + LY::SQ);
 
   const int tid = threadIdx.x;
@@ -162,9 +159,9 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
     bool ok = mbar_wait(q_full, 0, abort_flag);
     const float sq = sq_smem[r];
     const float rq = sq > 0.0f ? sq * kRowC : 1.0f;
-    const float cv = *cv_smem;
+    const float log2cv = *cv_smem;
     float m_run = -INFINITY;
-    float l_run = 0.0f;
+    float2 lacc = make_float2(0.0f, 0.0f);
     for (int j = 0; ok && j < T; ++j) {
       const int s = j % NSTAGE;
       const int b = j & 1;
@@ -173,86 +170,121 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         break;
       }
       tc_fence_after();
-      uint32_t sr[128];
-      tmem_ld32(tmem + lane_off + TM_S + b * 128 + 0, *reinterpret_cast<uint32_t(*)[32]>(sr + 0));
-      tmem_ld32(tmem + lane_off + TM_S + b * 128 + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
-      tmem_ld32(tmem + lane_off + TM_S + b * 128 + 64, *reinterpret_cast<uint32_t(*)[32]>(sr + 64));
-      tmem_ld32(tmem + lane_off + TM_S + b * 128 + 96, *reinterpret_cast<uint32_t(*)[32]>(sr + 96));
-      tmem_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s_empty[b]);
-
-      const float* skp = reinterpret_cast<const float*>(sm + LY::SK0 + s * BN * 4);
-      const float* svp = reinterpret_cast<const float*>(sm + LY::SV0 + s * BN * 4);
+      const float4* sk4 = reinterpret_cast<const float4*>(sm + LY::SK0 + s * BN * 4);
+      const float4* sv4 = reinterpret_cast<const float4*>(sm + LY::SV0 + s * BN * 4);
       const int valid = min(BN, n_valid - j * BN);
-      float t[128];
+      const uint32_t s_addr = tmem + lane_off + TM_S + b * 128;
+
+      // pass 1: the tile's row maximum of t = S * s_k
       float mt = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < 128; ++c) {
-        t[c] = c < valid ? __uint_as_float(sr[c]) * skp[c] : -INFINITY;
-        mt = fmaxf(mt, t[c]);
-      }
-      const float m_new = fmaxf(m_run, mt * rq);
-      const bool need = (j > 0) && (m_new > m_run);
-      if (__any_sync(0xFFFFFFFFu, need)) {
-        // O holds rows scaled by exp2(-m_run): bring them to exp2(-m_new)
-        if (!mbar_wait(&pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const float alpha = need ? ex2(m_run - m_new) : 1.0f;
+      for (int cb = 0; cb < 4; ++cb) {
+        uint32_t x[32];
+        tmem_ld32(s_addr + cb * 32, x);
+        tmem_wait_ld();
 #pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 16) {
-          uint32_t o[16];
-          tmem_ld16(tmem + lane_off + TM_O + c0, o);
-          tmem_wait_ld();
-#pragma unroll
-          for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-          tmem_st16(tmem + lane_off + TM_O + c0, o);
+        for (int i = 0; i < 32; i += 4) {
+          const float4 k4 = sk4[(cb * 32 + i) >> 2];
+          float2 t0 = mul2(make_float2(__uint_as_float(x[i]), __uint_as_float(x[i + 1])), make_float2(k4.x, k4.y));
+          float2 t1 = mul2(make_float2(__uint_as_float(x[i + 2]), __uint_as_float(x[i + 3])), make_float2(k4.z, k4.w));
+          if (valid < BN) {
+            const int c = cb * 32 + i;
+            if (c >= valid) t0.x = -INFINITY;
+            if (c + 1 >= valid) t0.y = -INFINITY;
+            if (c + 2 >= valid) t1.x = -INFINITY;
+            if (c + 3 >= valid) t1.y = -INFINITY;
+          }
+          mt = max3f(mt, t0.x, t0.y);
+          mt = max3f(mt, t1.x, t1.y);
         }
-        tmem_wait_st();
-        l_run *= alpha;
       }
-      m_run = m_new;
-
+      // raise the running maximum only when it is exceeded by more than 2^8
+      const float m_tile = mt * rq;
+      const bool grow = (j == 0) || (m_tile > m_run + kLazyRescale);
+      if (__any_sync(0xFFFFFFFFu, grow)) {
+        const float m_new = fmaxf(m_run, m_tile);
+        if (j > 0) {
+          // O holds rows weighted by exp2(-m_run): bring them to exp2(-m_new)
+          if (!mbar_wait(&pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const float alpha = ex2f(m_run - m_new);
+#pragma unroll
+          for (int c0 = 0; c0 < D; c0 += 16) {
+            uint32_t o[16];
+            tmem_ld16(tmem + lane_off + TM_O + c0, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tmem_st16(tmem + lane_off + TM_O + c0, o);
+          }
+          tmem_wait_st();
+          lacc.x *= alpha;
+          lacc.y *= alpha;
+        }
+        m_run = m_new;
+      }
       // P buffer b is free once PV of tile j-2 has finished
       if (j >= 2 && !mbar_wait(&pv_done[b], ((j - 2) >> 1) & 1, abort_flag)) {
         ok = false;
         break;
       }
-      uint8_t* pb = sm + LY::P0 + b * (BM * BN * 2);
-      float lsum = 0.0f;
+      tc_fence_after();
+      // pass 2: e = exp2(t*r - m + c), l += e, P = e * s_v -> fp16 -> TMEM
+      const float2 rq2 = make_float2(rq, rq);
+      const float2 moff = make_float2(log2cv - m_run, log2cv - m_run);
 #pragma unroll
-      for (int c8 = 0; c8 < 16; ++c8) {
-        uint32_t w[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int c = c8 * 8 + 2 * e;
-          const float p0 = ex2(fmaf(t[c], rq, -m_run));
-          const float p1 = ex2(fmaf(t[c + 1], rq, -m_run));
-          lsum += p0 + p1;
-          w[e] = cvt_f16x2(p0 * (svp[c] * cv), p1 * (svp[c + 1] * cv));
+      for (int cb = 0; cb < 4; ++cb) {
+        uint32_t x[32];
+        tmem_ld32(s_addr + cb * 32, x);
+        tmem_wait_ld();
+        if (cb == 3) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&s_empty[b]);
         }
-        const int ka = c8 >> 3;
-        const int cc = c8 & 7;
-        *reinterpret_cast<uint4*>(pb + ka * (BM * 128) + r * 128 + ((cc ^ (r & 7)) << 4)) =
-            make_uint4(w[0], w[1], w[2], w[3]);
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 32; i += 4) {
+          const float4 k4 = sk4[(cb * 32 + i) >> 2];
+          const float4 v4 = sv4[(cb * 32 + i) >> 2];
+          float2 t0 = mul2(make_float2(__uint_as_float(x[i]), __uint_as_float(x[i + 1])), make_float2(k4.x, k4.y));
+          float2 t1 = mul2(make_float2(__uint_as_float(x[i + 2]), __uint_as_float(x[i + 3])), make_float2(k4.z, k4.w));
+          t0 = fma2(t0, rq2, moff);
+          t1 = fma2(t1, rq2, moff);
+          float2 e0 = make_float2(ex2f(t0.x), ex2f(t0.y));
+          float2 e1 = make_float2(ex2f(t1.x), ex2f(t1.y));
+          if (valid < BN) {
+            const int c = cb * 32 + i;
+            if (c >= valid) e0.x = 0.0f;
+            if (c + 1 >= valid) e0.y = 0.0f;
+            if (c + 2 >= valid) e1.x = 0.0f;
+            if (c + 3 >= valid) e1.y = 0.0f;
+          }
+          lacc = add2(lacc, add2(e0, e1));
+          const float2 p0 = mul2(e0, make_float2(v4.x, v4.y));
+          const float2 p1 = mul2(e1, make_float2(v4.z, v4.w));
+          pk[i >> 1] = cvt_f16x2(p0.x, p0.y);
+          pk[(i >> 1) + 1] = cvt_f16x2(p1.x, p1.y);
+        }
+        tmem_st16(tmem + lane_off + TM_P + b * 64 + cb * 16, pk);
       }
-      l_run += lsum;
-      fence_proxy_async_smem();
+      tmem_wait_st();
+      tc_fence_before();
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(&p_full[b]);
         mbar_arrive(&kv_empty[s]);
       }
     }
-    // epilogue: out = O / (l * C_v)
+    const float l_run = lacc.x + lacc.y;
+    // epilogue: out = O / l
     if (ok && mbar_wait(&pv_done[(T - 1) & 1], ((T - 1) >> 1) & 1, abort_flag)) {
       tc_fence_after();
       const int qi = qt * BM + r;
-      const float scale = 1.0f / (l_run * cv);
+      const float scale = 1.0f / l_run;
       uint8_t* orow = static_cast<uint8_t*>(out) + ((size_t)qi * H + h) * (size_t)D * (out_f32 ? 4 : 2);
 #pragma unroll
       for (int c0 = 0; c0 < D; c0 += 16) {
@@ -328,8 +360,11 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
     asm volatile("bar.sync 1, 128;" ::: "memory");
     if (ct == 0) {
       const float m = __int_as_float(*maxsv_bits);
-      // C_v = 2^(14 - floor(log2 m)) so that max(s_v) * C_v < 2^15
-      *cv_smem = m > 0.0f ? exp2f((float)(14 - ilogbf(m))) : 1.0f;
+      // weights reach 2^8 * 2^c; with c = 6 - floor(log2 max s_v) every
+      // P = weight * s_v stays below 2^15 (fp16 max 65504)
+      int c = m > 0.0f ? 6 - ilogbf(m) : 0;
+      c = c < -64 ? -64 : (c > 64 ? 64 : c);
+      *cv_smem = (float)c;
     }
     asm volatile("bar.sync 1, 128;" ::: "memory");
     fence_proxy_async_smem();
@@ -344,11 +379,13 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       if (j >= 2 && !mbar_wait(&pv_done[b], ((j - 2) >> 1) & 1, abort_flag)) break;
       const uint8_t* vsrc = sm + LY::V0 + s * BN * D;
       uint8_t* vdst = sm + LY::VH0 + b * BN * D * 2;
+      // eight consecutive threads take the same chunk of eight consecutive
+      // slots, so their 16-byte reads and writes fall in distinct bank groups
 #pragma unroll
       for (int it = 0; it < BN * CH / 128; ++it) {
-        const int idx = it * 128 + ct;
-        const int sl = idx / CH;
-        const int c = idx % CH;
+        const int task = it * 128 + ct;
+        const int sl = 8 * (task / (8 * CH)) + (task & 7);
+        const int c = (task >> 3) % CH;
         const uint4 u = *reinterpret_cast<const uint4*>(vsrc + kmajor_chunk<D>(sl, c));
         uint4 o0, o1;
         o0.x = cvt_e4m3x2_to_f16x2((uint16_t)(u.x & 0xFFFFu));
@@ -399,12 +436,11 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         if (!mbar_wait(&p_full[b], (i >> 1) & 1, abort_flag) || !mbar_wait(&vh_full[b], (i >> 1) & 1, abort_flag))
           return false;
         tc_fence_after();
-        const uint32_t pa = smem_u32(sm + LY::P0 + b * BM * BN * 2);
         const uint32_t va = smem_u32(sm + LY::VH0 + b * BN * D * 2);
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
-          mma_f16_ss(tmem + TM_O, make_sdesc_sw128(pa + (kk >> 2) * (BM * 128) + (kk & 3) * 32, 16, 1024),
-                     make_sdesc_sw128(va + kk * 16 * 128, BN * 128, 1024), idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
+          mma_f16_ts(tmem + TM_O, tmem + TM_P + b * 64 + kk * 8, make_sdesc_sw128(va + kk * 16 * 128, BN * 128, 1024),
+                     idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&pv_done[b]);
         return true;
       };

@@ -6,27 +6,35 @@
 //
 // One block per (tile of 128 queries, head).  The slots are visited in tiles
 // of 128 in storage order: attention is a sum over the valid slots, so the
-// ring's wrap needs no reordering, and slots >= n_valid are masked.
+// ring's wrap needs no reordering, and slots >= n_valid are masked.  The
+// tiles are split between two streams (the first and the second half of the
+// tiles), each with its own softmax warpgroup, running maximum, running sum
+// and O accumulator; the two partial results are merged at the end.  While
+// one stream computes its softmax the tensor cores work for the other.
 //
 //   S_j  = Qcodes . Kcodes_j^T            tcgen05 kind::f8f6f4, fp32 in TMEM
 //   t    = S_j * s_k (per column);  logit*log2(e) = t * s_q * log2(e)/sqrt(D)
 //   online softmax in base 2: e = exp2(t*r - m + c), l += e, with a running
 //   row maximum m that is only raised (and O rescaled) when a tile's maximum
-//   exceeds it by more than 2^8, so e <= 2^8 * 2^c
-//   P    = e * s_v (per column) rounded to fp16, stored to TMEM
+//   exceeds it by more than 2^8, so e <= 2^8 * 2^c; each tile takes two
+//   passes over S (the maximum, then the weights)
+//   P    = e * s_v (per column) rounded to fp16, written over S_j in TMEM
 //   O   += P . Vcodes_j                    tcgen05 kind::f16 (A = P from TMEM)
-//   out  = O / l
+//   out  = (O_0 a_0 + O_1 a_1) / (l_0 a_0 + l_1 a_1),  a_i = exp2(m_i - max m)
 // The e4m3 V codes are widened to fp16 in shared memory (exact) because the
 // fp16 MMA takes both operands in fp16; P in fp16 keeps the weighted sum of V
 // within the accuracy that e4m3 weights would lose.  2^c is a per-head power of
 // two (cancelling between O and l) that keeps P within fp16 range.
 //
-// Warp roles (320 threads):
-//   warps 0-3  softmax + epilogue, thread r owns query row r (TMEM lane r)
-//   warps 4-7  prologue (RoPE + e4m3 of the 128 query rows, C_v), then the
-//              per-tile widening of V to fp16
-//   warp 8     TMA producer (K, V codes and their scales, 2 stages)
-//   warp 9     TMEM allocation and MMA issue
+// Warp roles (448 threads):
+//   warps 0-3   stream 0 softmax, thread r owns query row r (TMEM lane r)
+//   warps 4-7   stream 1 softmax, same rows; both groups first run the query
+//               prologue (RoPE + e4m3 of the 128 rows) and finally the merge,
+//               each for half of the output columns
+//   warps 8-11  the per-head fp16 range factor, then the per-tile widening
+//               of V to fp16
+//   warp 12     TMA producer (K, V codes and their scales, 4 stages)
+//   warp 13     TMEM allocation and MMA issue
 #include <cfloat>
 
 #include "common.cuh"
@@ -36,12 +44,12 @@ namespace kvring_dev {
 
 constexpr int BM = 128;           // query rows per block
 constexpr int BN = 128;           // slots per tile
-constexpr int NSTAGE = 2;         // fp8 K/V stages
-constexpr int ATT_THREADS = 320;
+constexpr int NSTAGE = 4;         // fp8 K/V stages
+constexpr int ATT_THREADS = 448;
+constexpr int SOFT_THREADS = 256;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t TM_S = 0;      // two fp32 S buffers at columns 0 and 128
-constexpr uint32_t TM_P = 256;    // two fp16 P buffers (64 columns each) at 256 and 320
-constexpr uint32_t TM_O = 384;    // fp32 O accumulator (D columns)
+constexpr uint32_t TM_S = 0;      // stream s: fp32 S / fp16 P at columns 128 s
+constexpr uint32_t TM_O = 256;    // stream s: fp32 O at columns 256 + 128 s
 constexpr float kLazyRescale = 8.0f;   // log2 of the largest unnormalised weight
 
 template <int D>
@@ -49,12 +57,13 @@ struct AttnLayout {
   static constexpr int Q = 0;                            // e4m3 [BM][D], K-major swizzled
   static constexpr int K0 = Q + BM * D;                  // NSTAGE x e4m3 [BN][D]
   static constexpr int V0 = K0 + NSTAGE * BN * D;        // NSTAGE x e4m3 [BN][D]
-  static constexpr int VH0 = V0 + NSTAGE * BN * D;       // 2 x fp16 [BN][D], MN-major swizzled
+  static constexpr int VH0 = V0 + NSTAGE * BN * D;       // per stream fp16 [BN][D], MN-major swizzled
   static constexpr int SK0 = VH0 + 2 * BN * D * 2;       // NSTAGE x fp32 [BN]
   static constexpr int SV0 = SK0 + NSTAGE * BN * 4;
   static constexpr int SQ = SV0 + NSTAGE * BN * 4;       // fp32 [BM]
-  static constexpr int BAR = SQ + BM * 4;
-  static constexpr int NBAR = 16;
+  static constexpr int ML = SQ + BM * 4;                 // fp32 [2 streams][2 (m, l)][BM]
+  static constexpr int BAR = ML + 4 * BM * 4;
+  static constexpr int NBAR = 2 * NSTAGE + 13;
   static constexpr int MISC = BAR + NBAR * 8;
   static constexpr int BYTES = MISC + 64;
   static constexpr int ALLOC = BYTES + 1024;             // slack for 1024-byte alignment
@@ -78,29 +87,124 @@ __device__ __forceinline__ uint64_t kmajor_desc(uint32_t addr) {
     return make_sdesc_sw64(addr, 16, 512);
 }
 
+// The tiles in the order the producer, the widening warps and the MMA issuer
+// walk them: (stream 0, tile 0), (stream 1, tile 0), (stream 0, tile 1), ...
+// Stream 0 owns tiles [0, T0), stream 1 tiles [T0, T), T0 = ceil(T/2); only
+// stream 0 can be one tile longer.
+struct TileSeq {
+  int T0, T1;
+  __device__ explicit TileSeq(int T) : T0((T + 1) >> 1), T1(T - ((T + 1) >> 1)) {}
+  __device__ int count() const { return T0 + T1; }
+  // position in the walk of (stream s, tile j of that stream)
+  __device__ int pos(int s, int j) const { return j < T1 ? 2 * j + s : 2 * T1 + (j - T1); }
+  __device__ void at(int u, int& s, int& j) const {
+    if (u < 2 * T1) {
+      s = u & 1;
+      j = u >> 1;
+    } else {
+      s = 0;
+      j = T1 + (u - 2 * T1);
+    }
+  }
+  __device__ int tile(int s, int j) const { return s * T0 + j; }
+};
+
+// Query rows [r0, r0 + 16) by one warp: lane l owns channels [l*C, l*C + C)
+// (C = D/32), loads are coalesced along the row; RoPE in fp32, the row's
+// absmax by shuffles, e4m3 codes into the K-major Q tile.
+template <int D>
+__device__ __forceinline__ void query_rows(const RingView& rv, const __nv_bfloat16* __restrict__ q,
+                                           const int32_t* __restrict__ q_pos, int n_q, int h, int qt, int r0,
+                                           uint8_t* qtile, float* sq_smem, bool& bad) {
+  constexpr int C = D / 32;     // channels per lane: 4 or 2
+  constexpr int PP = C / 2;     // pairs per lane
+  constexpr int R = 8;          // rows in flight per batch
+  const int lane = threadIdx.x & 31;
+  const int H = rv.H;
+#pragma unroll 1
+  for (int r1 = r0; r1 < r0 + 16; r1 += R) {
+    float x[R][C];
+    float2 cs[R][PP];
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+      const int qi = qt * BM + r1 + i;
+      if (qi < n_q) {
+        const __nv_bfloat16* src = q + ((size_t)qi * H + h) * D + lane * C;
+        if constexpr (C == 4) {
+          const uint2 u = __ldg(reinterpret_cast<const uint2*>(src));
+          x[i][0] = __uint_as_float(u.x << 16);
+          x[i][1] = __uint_as_float(u.x & 0xFFFF0000u);
+          x[i][2] = __uint_as_float(u.y << 16);
+          x[i][3] = __uint_as_float(u.y & 0xFFFF0000u);
+        } else {
+          const uint32_t u = __ldg(reinterpret_cast<const uint32_t*>(src));
+          x[i][0] = __uint_as_float(u << 16);
+          x[i][1] = __uint_as_float(u & 0xFFFF0000u);
+        }
+        const int32_t* pr = q_pos + (size_t)qi * rv.n_axes;
+#pragma unroll
+        for (int m = 0; m < PP; ++m) cs[i][m] = rope_cs(rv, pr, lane * PP + m, bad);
+      } else {
+#pragma unroll
+        for (int m = 0; m < C; ++m) x[i][m] = 0.0f;
+#pragma unroll
+        for (int m = 0; m < PP; ++m) cs[i][m] = make_float2(1.0f, 0.0f);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+      const int r = r1 + i;
+#pragma unroll
+      for (int m = 0; m < PP; ++m) rope_pair(x[i][2 * m], x[i][2 * m + 1], cs[i][m].x, cs[i][m].y);
+      float amax = 0.0f;
+#pragma unroll
+      for (int m = 0; m < C; ++m) amax = fmaxf(amax, fabsf(x[i][m]));
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
+      float scale, inv;
+      absmax_scale(amax, scale, inv);
+      uint32_t codes = 0;
+      if (inv != 0.0f) {
+        codes = cvt_e4m3x2(__fmul_rn(x[i][0], inv), __fmul_rn(x[i][1], inv));
+        if constexpr (C == 4) codes |= (uint32_t)cvt_e4m3x2(__fmul_rn(x[i][2], inv), __fmul_rn(x[i][3], inv)) << 16;
+      }
+      const int byte = lane * C;   // channel offset = byte offset of the codes
+      uint8_t* dst = qtile + kmajor_chunk<D>(r, byte >> 4) + (byte & 15);
+      if constexpr (C == 4)
+        *reinterpret_cast<uint32_t*>(dst) = codes;
+      else
+        *reinterpret_cast<uint16_t*>(dst) = (uint16_t)codes;
+      if (lane == 0) sq_smem[r] = scale;
+    }
+  }
+}
+
 template <int D>
 __global__ void __launch_bounds__(ATT_THREADS, 1)
     fp8_ring_attn_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                          const __grid_constant__ CUtensorMap tmSK, const __grid_constant__ CUtensorMap tmSV,
-                         RingView rv, const uint4* __restrict__ q, const int32_t* __restrict__ q_pos, int n_q,
-                         void* __restrict__ out, int out_f32) {
+                         RingView rv, const __nv_bfloat16* __restrict__ q, const int32_t* __restrict__ q_pos,
+                         int n_q, void* __restrict__ out, int out_f32) {
   using LY = AttnLayout<D>;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // 1024-byte aligned base, derived by offsetting the __shared__ array itself
+  // so the compiler keeps every access below in the shared address space
+  uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + LY::BAR);
-  uint64_t* kv_full = bars + 0;
-  uint64_t* kv_empty = bars + 2;
-  uint64_t* s_full = bars + 4;
-  uint64_t* s_empty = bars + 6;
-  uint64_t* vh_full = bars + 8;
-  uint64_t* p_full = bars + 10;
-  uint64_t* pv_done = bars + 12;
-  uint64_t* q_full = bars + 14;
+  uint64_t* kv_full = bars + 0;                 // [NSTAGE]
+  uint64_t* kv_empty = bars + NSTAGE;           // [NSTAGE]
+  uint64_t* s_full = bars + 2 * NSTAGE;         // [2 streams]
+  uint64_t* vh_full = s_full + 2;               // [2 streams]
+  uint64_t* p_full = s_full + 4;                // [2 streams]
+  uint64_t* pv_done = s_full + 6;               // [2 streams]
+  uint64_t* q_full = s_full + 8;
+  uint64_t* ml_xchg = s_full + 9;               // [4 warp pairs]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + LY::MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + LY::MISC + 4);
   int* maxsv_bits = reinterpret_cast<int*>(sm + LY::MISC + 8);
   float* cv_smem = reinterpret_cast<float*>(sm + LY::MISC + 12);   // log2 of the per-head weight factor
   float* sq_smem = reinterpret_cast<float*>(sm + LY::SQ);
+  float* ml = reinterpret_cast<float*>(sm + LY::ML);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -110,27 +214,30 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
   const int H = rv.H;
   const int n_valid = rv.state[ST_NVALID];
   const int T = (n_valid + BN - 1) / BN;
+  const TileSeq seq(T);
 
   if (tid == 0) {
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < NSTAGE; ++i) {
       mbar_init(&kv_full[i], 1);
-      mbar_init(&kv_empty[i], 1 + 4 + 4);
+      mbar_init(&kv_empty[i], 1 + 4 + 4);   // QK commit, 4 widening warps, 4 softmax warps
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&s_empty[i], 4);
       mbar_init(&vh_full[i], 4);
       mbar_init(&p_full[i], 4);
       mbar_init(&pv_done[i], 1);
     }
-    mbar_init(q_full, 4);
+    mbar_init(q_full, 12);
+    for (int i = 0; i < 4; ++i) mbar_init(&ml_xchg[i], 2);
     *abort_flag = 0;
     *maxsv_bits = 0;
     fence_mbar_init();
   }
-  if (warp == 9) {
+  if (warp == 13) {
     tmem_alloc(tmem_slot, TMEM_COLS);
     tmem_relinquish();
   }
-  if (warp == 8 && lane == 0) {
+  if (warp == 12 && lane == 0) {
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
     tma_prefetch_desc(&tmSK);
@@ -142,7 +249,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
 
   if (n_valid <= 0) {
     // nothing to attend to: zeros, and a flag the host can read
-    if (warp < 4) {
+    if (tid < BM) {
       const int qi = qt * BM + tid;
       if (qi < n_q) {
         const int bytes = D * (out_f32 ? 4 : 2);
@@ -151,74 +258,90 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       }
     }
     if (tid == 0 && qt == 0 && h == 0) atomicOr(&rv.state[ST_ERR], DEVERR_EMPTY);
-  } else if (warp < 4) {
-    // ======================================================== softmax + epilogue
-    const int r = tid;
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+  } else if (warp < 8) {
+    // ======================================================== query prologue
+    {
+      bool bad = false;
+      query_rows<D>(rv, q, q_pos, n_q, h, qt, warp * 16, sm + LY::Q, sq_smem, bad);
+      if (bad) atomicOr(&rv.state[ST_ERR], DEVERR_POS_RANGE);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(q_full);
+    }
+    // ======================================================== softmax of stream g
+    const int g = warp >> 2;
+    const int r = tid & 127;                     // query row = TMEM lane
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t s_addr = tmem + lane_off + TM_S + g * 128;
+    const uint32_t o_addr = tmem + lane_off + TM_O + g * 128;
     constexpr float kRowC = (D == 128 ? 0.08838834764831845f : 0.125f) * 1.4426950408889634f;
     bool ok = mbar_wait(q_full, 0, abort_flag);
     const float sq = sq_smem[r];
     const float rq = sq > 0.0f ? sq * kRowC : 1.0f;
     const float log2cv = *cv_smem;
+    const float2 rq2 = make_float2(rq, rq);
+    const int Tg = g == 0 ? seq.T0 : seq.T1;
     float m_run = -INFINITY;
     float2 lacc = make_float2(0.0f, 0.0f);
-    for (int j = 0; ok && j < T; ++j) {
-      const int s = j % NSTAGE;
-      const int b = j & 1;
-      if (!mbar_wait(&kv_full[s], (j / NSTAGE) & 1, abort_flag) || !mbar_wait(&s_full[b], (j >> 1) & 1, abort_flag)) {
+    for (int j = 0; ok && j < Tg; ++j) {
+      const int u = seq.pos(g, j);
+      const int st = u % NSTAGE;
+      if (!mbar_wait(&kv_full[st], (u / NSTAGE) & 1, abort_flag) || !mbar_wait(&s_full[g], j & 1, abort_flag)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const float4* sk4 = reinterpret_cast<const float4*>(sm + LY::SK0 + s * BN * 4);
-      const float4* sv4 = reinterpret_cast<const float4*>(sm + LY::SV0 + s * BN * 4);
-      const int valid = min(BN, n_valid - j * BN);
-      const uint32_t s_addr = tmem + lane_off + TM_S + b * 128;
-
-      // pass 1: the tile's row maximum of t = S * s_k
+      const float4* sk4 = reinterpret_cast<const float4*>(sm + LY::SK0 + st * BN * 4);
+      const float4* sv4 = reinterpret_cast<const float4*>(sm + LY::SV0 + st * BN * 4);
+      const int valid = min(BN, n_valid - seq.tile(g, j) * BN);
+      // Pass 1: the tile's row maximum of t = S * s_k.  If it exceeds the
+      // running maximum by more than 2^8 (always on the first tile), raise the
+      // maximum and rescale O.  Pass 2: the weights, whose fp16 P is written
+      // over the S columns this pass has already read.  The chunk loops are
+      // kept rolled: an unrolled body does not fit the instruction cache.
       float mt = -INFINITY;
-#pragma unroll
+#pragma unroll 1
       for (int cb = 0; cb < 4; ++cb) {
         uint32_t x[32];
         tmem_ld32(s_addr + cb * 32, x);
         tmem_wait_ld();
+        const float4* k4p = sk4 + cb * 8;
+        const int vc = valid - cb * 32;
 #pragma unroll
         for (int i = 0; i < 32; i += 4) {
-          const float4 k4 = sk4[(cb * 32 + i) >> 2];
+          const float4 k4 = k4p[i >> 2];
           float2 t0 = mul2(make_float2(__uint_as_float(x[i]), __uint_as_float(x[i + 1])), make_float2(k4.x, k4.y));
           float2 t1 = mul2(make_float2(__uint_as_float(x[i + 2]), __uint_as_float(x[i + 3])), make_float2(k4.z, k4.w));
-          if (valid < BN) {
-            const int c = cb * 32 + i;
-            if (c >= valid) t0.x = -INFINITY;
-            if (c + 1 >= valid) t0.y = -INFINITY;
-            if (c + 2 >= valid) t1.x = -INFINITY;
-            if (c + 3 >= valid) t1.y = -INFINITY;
+          if (vc < 32) {
+            if (i >= vc) t0.x = -INFINITY;
+            if (i + 1 >= vc) t0.y = -INFINITY;
+            if (i + 2 >= vc) t1.x = -INFINITY;
+            if (i + 3 >= vc) t1.y = -INFINITY;
           }
           mt = max3f(mt, t0.x, t0.y);
           mt = max3f(mt, t1.x, t1.y);
         }
       }
-      // raise the running maximum only when it is exceeded by more than 2^8
       const float m_tile = mt * rq;
       const bool grow = (j == 0) || (m_tile > m_run + kLazyRescale);
       if (__any_sync(0xFFFFFFFFu, grow)) {
         const float m_new = fmaxf(m_run, m_tile);
         if (j > 0) {
           // O holds rows weighted by exp2(-m_run): bring them to exp2(-m_new)
-          if (!mbar_wait(&pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag)) {
+          if (!mbar_wait(&pv_done[g], (j - 1) & 1, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const float alpha = ex2f(m_run - m_new);
-#pragma unroll
+#pragma unroll 1
           for (int c0 = 0; c0 < D; c0 += 16) {
             uint32_t o[16];
-            tmem_ld16(tmem + lane_off + TM_O + c0, o);
+            tmem_ld16(o_addr + c0, o);
             tmem_wait_ld();
 #pragma unroll
             for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-            tmem_st16(tmem + lane_off + TM_O + c0, o);
+            tmem_st16(o_addr + c0, o);
           }
           tmem_wait_st();
           lacc.x *= alpha;
@@ -226,42 +349,31 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         }
         m_run = m_new;
       }
-      // P buffer b is free once PV of tile j-2 has finished
-      if (j >= 2 && !mbar_wait(&pv_done[b], ((j - 2) >> 1) & 1, abort_flag)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      // pass 2: e = exp2(t*r - m + c), l += e, P = e * s_v -> fp16 -> TMEM
-      const float2 rq2 = make_float2(rq, rq);
       const float2 moff = make_float2(log2cv - m_run, log2cv - m_run);
-#pragma unroll
+#pragma unroll 1
       for (int cb = 0; cb < 4; ++cb) {
         uint32_t x[32];
         tmem_ld32(s_addr + cb * 32, x);
         tmem_wait_ld();
-        if (cb == 3) {
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&s_empty[b]);
-        }
+        const float4* k4p = sk4 + cb * 8;
+        const float4* v4p = sv4 + cb * 8;
+        const int vc = valid - cb * 32;
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 32; i += 4) {
-          const float4 k4 = sk4[(cb * 32 + i) >> 2];
-          const float4 v4 = sv4[(cb * 32 + i) >> 2];
+          const float4 k4 = k4p[i >> 2];
+          const float4 v4 = v4p[i >> 2];
           float2 t0 = mul2(make_float2(__uint_as_float(x[i]), __uint_as_float(x[i + 1])), make_float2(k4.x, k4.y));
           float2 t1 = mul2(make_float2(__uint_as_float(x[i + 2]), __uint_as_float(x[i + 3])), make_float2(k4.z, k4.w));
           t0 = fma2(t0, rq2, moff);
           t1 = fma2(t1, rq2, moff);
           float2 e0 = make_float2(ex2f(t0.x), ex2f(t0.y));
           float2 e1 = make_float2(ex2f(t1.x), ex2f(t1.y));
-          if (valid < BN) {
-            const int c = cb * 32 + i;
-            if (c >= valid) e0.x = 0.0f;
-            if (c + 1 >= valid) e0.y = 0.0f;
-            if (c + 2 >= valid) e1.x = 0.0f;
-            if (c + 3 >= valid) e1.y = 0.0f;
+          if (vc < 32) {
+            if (i >= vc) e0.x = 0.0f;
+            if (i + 1 >= vc) e0.y = 0.0f;
+            if (i + 2 >= vc) e1.x = 0.0f;
+            if (i + 3 >= vc) e1.y = 0.0f;
           }
           lacc = add2(lacc, add2(e0, e1));
           const float2 p0 = mul2(e0, make_float2(v4.x, v4.y));
@@ -269,116 +381,123 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
           pk[i >> 1] = cvt_f16x2(p0.x, p0.y);
           pk[(i >> 1) + 1] = cvt_f16x2(p1.x, p1.y);
         }
-        tmem_st16(tmem + lane_off + TM_P + b * 64 + cb * 16, pk);
+        tmem_st16(s_addr + cb * 16, pk);
       }
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(&p_full[b]);
-        mbar_arrive(&kv_empty[s]);
+        mbar_arrive(&p_full[g]);
+        mbar_arrive(&kv_empty[st]);
       }
     }
-    const float l_run = lacc.x + lacc.y;
-    // epilogue: out = O / l
-    if (ok && mbar_wait(&pv_done[(T - 1) & 1], ((T - 1) >> 1) & 1, abort_flag)) {
+    // ======================================================== merge + epilogue
+    // Warps w and w+4 hold the same rows: they swap (m, l), then each writes
+    // half of the output columns from both streams' O.
+    float* mine = ml + g * 2 * BM;
+    float* other = ml + (g ^ 1) * 2 * BM;
+    const float l_mine = lacc.x + lacc.y;
+    mine[r] = m_run;
+    mine[BM + r] = l_mine;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&ml_xchg[warp & 3]);
+    ok = ok && mbar_wait(&ml_xchg[warp & 3], 0, abort_flag);
+    const float m_o = other[r];
+    const float l_o = other[BM + r];
+    const float m0 = g == 0 ? m_run : m_o;
+    const float m1 = g == 0 ? m_o : m_run;
+    const float l0 = g == 0 ? l_mine : l_o;
+    const float l1 = g == 0 ? l_o : l_mine;
+    const bool has1 = seq.T1 > 0;
+    ok = ok && mbar_wait(&pv_done[0], (seq.T0 - 1) & 1, abort_flag);
+    ok = ok && (!has1 || mbar_wait(&pv_done[1], (seq.T1 - 1) & 1, abort_flag));
+    if (ok) {
       tc_fence_after();
+      const float M = has1 ? fmaxf(m0, m1) : m0;
+      const float a0 = ex2f(m0 - M);
+      const float a1 = has1 ? ex2f(m1 - M) : 0.0f;
+      const float inv_l = 1.0f / (l0 * a0 + l1 * a1);
+      const float w0 = a0 * inv_l;
+      const float w1 = a1 * inv_l;
       const int qi = qt * BM + r;
-      const float scale = 1.0f / l_run;
+      const uint32_t o0_addr = tmem + lane_off + TM_O;
+      const uint32_t o1_addr = tmem + lane_off + TM_O + 128;
       uint8_t* orow = static_cast<uint8_t*>(out) + ((size_t)qi * H + h) * (size_t)D * (out_f32 ? 4 : 2);
-#pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 16) {
-        uint32_t o[16];
-        tmem_ld16(tmem + lane_off + TM_O + c0, o);
+#pragma unroll 1
+      for (int c0 = g * (D / 2); c0 < (g + 1) * (D / 2); c0 += 16) {
+        uint32_t o0[16], o1[16];
+        tmem_ld16(o0_addr + c0, o0);
+        tmem_ld16(o1_addr + c0, o1);
         tmem_wait_ld();
+        float v[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          v[i] = has1 ? __uint_as_float(o0[i]) * w0 + __uint_as_float(o1[i]) * w1 : __uint_as_float(o0[i]) * w0;
         if (qi < n_q) {
           if (out_f32) {
             uint4* dst = reinterpret_cast<uint4*>(orow + c0 * 4);
 #pragma unroll
             for (int i = 0; i < 4; ++i)
-              dst[i] = make_uint4(__float_as_uint(__uint_as_float(o[4 * i]) * scale),
-                                  __float_as_uint(__uint_as_float(o[4 * i + 1]) * scale),
-                                  __float_as_uint(__uint_as_float(o[4 * i + 2]) * scale),
-                                  __float_as_uint(__uint_as_float(o[4 * i + 3]) * scale));
+              dst[i] = make_uint4(__float_as_uint(v[4 * i]), __float_as_uint(v[4 * i + 1]),
+                                  __float_as_uint(v[4 * i + 2]), __float_as_uint(v[4 * i + 3]));
           } else {
-            uint32_t pk[8];
+            uint32_t pb[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-              const __nv_bfloat162 v2 =
-                  __floats2bfloat162_rn(__uint_as_float(o[2 * i]) * scale, __uint_as_float(o[2 * i + 1]) * scale);
-              pk[i] = *reinterpret_cast<const uint32_t*>(&v2);
+              const __nv_bfloat162 v2 = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+              pb[i] = *reinterpret_cast<const uint32_t*>(&v2);
             }
             uint4* dst = reinterpret_cast<uint4*>(orow + c0 * 2);
-            dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-            dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+            dst[0] = make_uint4(pb[0], pb[1], pb[2], pb[3]);
+            dst[1] = make_uint4(pb[4], pb[5], pb[6], pb[7]);
           }
         }
       }
     }
     tc_fence_before();
-  } else if (warp < 8) {
-    // ======================================================== prologue + V widening
-    const int ct = tid - 128;
-    // C_v from the largest V scale of this head
-    float mx = 0.0f;
-    const float* vs = rv.v_scale + (size_t)h * rv.S_pad;
-    for (int i = ct; i < n_valid; i += 128) mx = fmaxf(mx, vs[i]);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
-    if (lane == 0) atomicMax(maxsv_bits, __float_as_int(mx));
-
-    // query row ct: RoPE in fp32, e4m3 with its own absmax scale
-    const int qi = qt * BM + ct;
-    uint8_t* qtile = sm + LY::Q;
-    float sq = 0.0f;
-    bool bad = false;
-    if (qi < n_q) {
-      float x[D];
-      const uint4* src = q + ((size_t)qi * H + h) * (D / 8);
-#pragma unroll
-      for (int i = 0; i < D / 8; ++i) bf16x8_to_f32(__ldg(src + i), x + 8 * i);
-      const int32_t* pr = q_pos + (size_t)qi * rv.n_axes;
-#pragma unroll
-      for (int p = 0; p < D / 2; ++p) {
-        const float2 cs = rope_cs(rv, pr, p, bad);
-        rope_pair(x[2 * p], x[2 * p + 1], cs.x, cs.y);
+  } else if (warp < 12) {
+    // ======================================================== range factor + V widening
+    const int ct = tid - SOFT_THREADS;
+    {
+      // the largest V scale of this head (each head's scale row starts
+      // 16-byte aligned: rows are S_pad = S rounded up to 4 apart)
+      const float* vs1 = rv.v_scale + (size_t)h * rv.S_pad;
+      const float4* vs = reinterpret_cast<const float4*>(vs1);
+      const int n4 = n_valid >> 2;
+      float mx = 0.0f;
+#pragma unroll 4
+      for (int i = ct; i < n4; i += 128) {
+        const float4 v = __ldg(vs + i);
+        mx = fmaxf(mx, fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
       }
-      float amax = 0.0f;
+      if (ct < (n_valid & 3)) mx = fmaxf(mx, vs1[n4 * 4 + ct]);
 #pragma unroll
-      for (int i = 0; i < D; ++i) amax = fmaxf(amax, fabsf(x[i]));
-      float inv;
-      absmax_scale(amax, sq, inv);
-#pragma unroll
-      for (int c = 0; c < D / 16; ++c)
-        *reinterpret_cast<uint4*>(qtile + kmajor_chunk<D>(ct, c)) = quant16(x + 16 * c, inv);
-    } else {
-#pragma unroll
-      for (int c = 0; c < D / 16; ++c) *reinterpret_cast<uint4*>(qtile + kmajor_chunk<D>(ct, c)) = make_uint4(0, 0, 0, 0);
+      for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
+      if (lane == 0) atomicMax(maxsv_bits, __float_as_int(mx));
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+      if (ct == 0) {
+        const float m = __int_as_float(*maxsv_bits);
+        // weights reach 2^8 * 2^c; with c = 6 - floor(log2 max s_v) every
+        // P = weight * s_v stays below 2^15 (fp16 max 65504)
+        int c = m > 0.0f ? 6 - ilogbf(m) : 0;
+        c = c < -64 ? -64 : (c > 64 ? 64 : c);
+        *cv_smem = (float)c;
+      }
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) mbar_arrive(q_full);
     }
-    sq_smem[ct] = sq;
-    if (bad) atomicOr(&rv.state[ST_ERR], DEVERR_POS_RANGE);
-    asm volatile("bar.sync 1, 128;" ::: "memory");
-    if (ct == 0) {
-      const float m = __int_as_float(*maxsv_bits);
-      // weights reach 2^8 * 2^c; with c = 6 - floor(log2 max s_v) every
-      // P = weight * s_v stays below 2^15 (fp16 max 65504)
-      int c = m > 0.0f ? 6 - ilogbf(m) : 0;
-      c = c < -64 ? -64 : (c > 64 ? 64 : c);
-      *cv_smem = (float)c;
-    }
-    asm volatile("bar.sync 1, 128;" ::: "memory");
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(q_full);
 
     constexpr int CH = D / 16;  // 16-byte e4m3 chunks per slot row
-    for (int j = 0; j < T; ++j) {
-      const int s = j % NSTAGE;
-      const int b = j & 1;
-      if (!mbar_wait(&kv_full[s], (j / NSTAGE) & 1, abort_flag)) break;
-      if (j >= 2 && !mbar_wait(&pv_done[b], ((j - 2) >> 1) & 1, abort_flag)) break;
-      const uint8_t* vsrc = sm + LY::V0 + s * BN * D;
-      uint8_t* vdst = sm + LY::VH0 + b * BN * D * 2;
+    for (int u = 0; u < seq.count(); ++u) {
+      int sg, j;
+      seq.at(u, sg, j);
+      const int st = u % NSTAGE;
+      if (!mbar_wait(&kv_full[st], (u / NSTAGE) & 1, abort_flag)) break;
+      // the stream's fp16 V buffer is free once its previous PV has finished
+      if (j >= 1 && !mbar_wait(&pv_done[sg], (j - 1) & 1, abort_flag)) break;
+      const uint8_t* vsrc = sm + LY::V0 + st * BN * D;
+      uint8_t* vdst = sm + LY::VH0 + sg * BN * D * 2;
       // eight consecutive threads take the same chunk of eight consecutive
       // slots, so their 16-byte reads and writes fall in distinct bank groups
 #pragma unroll
@@ -386,16 +505,16 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         const int task = it * 128 + ct;
         const int sl = 8 * (task / (8 * CH)) + (task & 7);
         const int c = (task >> 3) % CH;
-        const uint4 u = *reinterpret_cast<const uint4*>(vsrc + kmajor_chunk<D>(sl, c));
+        const uint4 w = *reinterpret_cast<const uint4*>(vsrc + kmajor_chunk<D>(sl, c));
         uint4 o0, o1;
-        o0.x = cvt_e4m3x2_to_f16x2((uint16_t)(u.x & 0xFFFFu));
-        o0.y = cvt_e4m3x2_to_f16x2((uint16_t)(u.x >> 16));
-        o0.z = cvt_e4m3x2_to_f16x2((uint16_t)(u.y & 0xFFFFu));
-        o0.w = cvt_e4m3x2_to_f16x2((uint16_t)(u.y >> 16));
-        o1.x = cvt_e4m3x2_to_f16x2((uint16_t)(u.z & 0xFFFFu));
-        o1.y = cvt_e4m3x2_to_f16x2((uint16_t)(u.z >> 16));
-        o1.z = cvt_e4m3x2_to_f16x2((uint16_t)(u.w & 0xFFFFu));
-        o1.w = cvt_e4m3x2_to_f16x2((uint16_t)(u.w >> 16));
+        o0.x = cvt_e4m3x2_to_f16x2((uint16_t)(w.x & 0xFFFFu));
+        o0.y = cvt_e4m3x2_to_f16x2((uint16_t)(w.x >> 16));
+        o0.z = cvt_e4m3x2_to_f16x2((uint16_t)(w.y & 0xFFFFu));
+        o0.w = cvt_e4m3x2_to_f16x2((uint16_t)(w.y >> 16));
+        o1.x = cvt_e4m3x2_to_f16x2((uint16_t)(w.z & 0xFFFFu));
+        o1.y = cvt_e4m3x2_to_f16x2((uint16_t)(w.z >> 16));
+        o1.z = cvt_e4m3x2_to_f16x2((uint16_t)(w.w & 0xFFFFu));
+        o1.w = cvt_e4m3x2_to_f16x2((uint16_t)(w.w >> 16));
         // channels 16c .. 16c+15 -> MN-major fp16 tile: 64-channel column
         // blocks of [BN][128 bytes], 128-byte swizzle by slot
         const int d0 = 16 * c;
@@ -407,68 +526,78 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(&vh_full[b]);
-        mbar_arrive(&kv_empty[s]);
+        mbar_arrive(&vh_full[sg]);
+        mbar_arrive(&kv_empty[st]);
       }
     }
-  } else if (warp == 8) {
+  } else if (warp == 12) {
     // ======================================================== TMA producer
     if (lane == 0) {
-      for (int j = 0; j < T; ++j) {
-        const int s = j % NSTAGE;
-        if (j >= NSTAGE && !mbar_wait(&kv_empty[s], ((j / NSTAGE) - 1) & 1, abort_flag)) break;
-        mbar_arrive_expect_tx(&kv_full[s], 2 * BN * D + 2 * BN * 4);
-        tma_load_3d(sm + LY::K0 + s * BN * D, &tmK, &kv_full[s], 0, j * BN, h);
-        tma_load_3d(sm + LY::V0 + s * BN * D, &tmV, &kv_full[s], 0, j * BN, h);
-        tma_load_2d(sm + LY::SK0 + s * BN * 4, &tmSK, &kv_full[s], j * BN, h);
-        tma_load_2d(sm + LY::SV0 + s * BN * 4, &tmSV, &kv_full[s], j * BN, h);
+      for (int u = 0; u < seq.count(); ++u) {
+        int sg, j;
+        seq.at(u, sg, j);
+        const int st = u % NSTAGE;
+        if (u >= NSTAGE && !mbar_wait(&kv_empty[st], ((u / NSTAGE) - 1) & 1, abort_flag)) break;
+        const int t = seq.tile(sg, j);
+        mbar_arrive_expect_tx(&kv_full[st], 2 * BN * D + 2 * BN * 4);
+        tma_load_3d(sm + LY::K0 + st * BN * D, &tmK, &kv_full[st], 0, t * BN, h);
+        tma_load_3d(sm + LY::V0 + st * BN * D, &tmV, &kv_full[st], 0, t * BN, h);
+        tma_load_2d(sm + LY::SK0 + st * BN * 4, &tmSK, &kv_full[st], t * BN, h);
+        tma_load_2d(sm + LY::SV0 + st * BN * 4, &tmSV, &kv_full[st], t * BN, h);
       }
     }
   } else {
     // ======================================================== MMA issue
+    // Order: QK of both streams' first tiles, then per tile index j:
+    // PV_0(j), QK_0(j+1), PV_1(j), QK_1(j+1).  QK_s(j+1) overwrites the
+    // buffer PV_s(j) reads P from, so it waits for PV_s(j) to finish.
     if (lane == 0) {
       constexpr uint32_t idesc_qk = make_idesc(0, 0, 0, 0, BM, BN);   // e4m3 x e4m3, both K-major
       constexpr uint32_t idesc_pv = make_idesc(0, 0, 0, 1, BM, D);    // f16 x f16, V MN-major
       bool ok = mbar_wait(q_full, 0, abort_flag);
       const uint32_t q_addr = smem_u32(sm + LY::Q);
-      auto issue_pv = [&](int i) -> bool {
-        const int b = i & 1;
-        if (!mbar_wait(&p_full[b], (i >> 1) & 1, abort_flag) || !mbar_wait(&vh_full[b], (i >> 1) & 1, abort_flag))
-          return false;
+      auto issue_qk = [&](int sg, int j) -> bool {
+        const int u = seq.pos(sg, j);
+        const int st = u % NSTAGE;
+        if (!mbar_wait(&kv_full[st], (u / NSTAGE) & 1, abort_flag)) return false;
+        if (j >= 1 && !mbar_wait(&pv_done[sg], (j - 1) & 1, abort_flag)) return false;
         tc_fence_after();
-        const uint32_t va = smem_u32(sm + LY::VH0 + b * BN * D * 2);
-#pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk)
-          mma_f16_ts(tmem + TM_O, tmem + TM_P + b * 64 + kk * 8, make_sdesc_sw128(va + kk * 16 * 128, BN * 128, 1024),
-                     idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&pv_done[b]);
-        return true;
-      };
-      for (int j = 0; ok && j < T; ++j) {
-        const int s = j % NSTAGE;
-        const int b = j & 1;
-        if (!mbar_wait(&kv_full[s], (j / NSTAGE) & 1, abort_flag) ||
-            (j >= 2 && !mbar_wait(&s_empty[b], ((j >> 1) - 1) & 1, abort_flag))) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t ka = smem_u32(sm + LY::K0 + s * BN * D);
+        const uint32_t ka = smem_u32(sm + LY::K0 + st * BN * D);
 #pragma unroll
         for (int kk = 0; kk < D / 32; ++kk)
-          mma_f8_ss(tmem + TM_S + b * 128, kmajor_desc<D>(q_addr + kk * 32), kmajor_desc<D>(ka + kk * 32), idesc_qk,
+          mma_f8_ss(tmem + TM_S + sg * 128, kmajor_desc<D>(q_addr + kk * 32), kmajor_desc<D>(ka + kk * 32), idesc_qk,
                     kk > 0 ? 1u : 0u);
-        mma_commit(&s_full[b]);
-        mma_commit(&kv_empty[s]);
-        if (j >= 1 && !issue_pv(j - 1)) ok = false;
+        mma_commit(&s_full[sg]);
+        mma_commit(&kv_empty[st]);
+        return true;
+      };
+      auto issue_pv = [&](int sg, int j) -> bool {
+        if (!mbar_wait(&p_full[sg], j & 1, abort_flag) || !mbar_wait(&vh_full[sg], j & 1, abort_flag)) return false;
+        tc_fence_after();
+        const uint32_t va = smem_u32(sm + LY::VH0 + sg * BN * D * 2);
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk)
+          mma_f16_ts(tmem + TM_O + sg * 128, tmem + TM_S + sg * 128 + kk * 8,
+                     make_sdesc_sw128(va + kk * 16 * 128, BN * 128, 1024), idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&pv_done[sg]);
+        return true;
+      };
+      ok = ok && issue_qk(0, 0);
+      if (seq.T1 > 0) ok = ok && issue_qk(1, 0);
+      for (int j = 0; ok && j < seq.T0; ++j) {
+        ok = ok && issue_pv(0, j);
+        if (j + 1 < seq.T0) ok = ok && issue_qk(0, j + 1);
+        if (j < seq.T1) {
+          ok = ok && issue_pv(1, j);
+          if (j + 1 < seq.T1) ok = ok && issue_qk(1, j + 1);
+        }
       }
-      if (ok) issue_pv(T - 1);
     }
   }
 
   __syncthreads();
   if (tid == 0 && *abort_flag) atomicOr(&rv.state[ST_ERR], DEVERR_TIMEOUT);
-  if (warp == 9) {
+  if (warp == 13) {
     tc_fence_after();
     tmem_dealloc(tmem, TMEM_COLS);
   }
@@ -485,14 +614,13 @@ cudaError_t prepare_attend(int D) {
 cudaError_t launch_fp8_ring_attn(const RingView& rv, const AttnMaps& maps, const void* q, const int32_t* q_pos,
                                  int n_q, void* out, int out_f32, cudaStream_t st) {
   const dim3 grid((n_q + BM - 1) / BM, rv.H);
+  const __nv_bfloat16* qb = static_cast<const __nv_bfloat16*>(q);
   if (rv.D == 128)
     fp8_ring_attn_kernel<128><<<grid, ATT_THREADS, AttnLayout<128>::ALLOC, st>>>(
-        maps.k_codes, maps.v_codes, maps.k_scale, maps.v_scale, rv, static_cast<const uint4*>(q), q_pos, n_q, out,
-        out_f32);
+        maps.k_codes, maps.v_codes, maps.k_scale, maps.v_scale, rv, qb, q_pos, n_q, out, out_f32);
   else
     fp8_ring_attn_kernel<64><<<grid, ATT_THREADS, AttnLayout<64>::ALLOC, st>>>(
-        maps.k_codes, maps.v_codes, maps.k_scale, maps.v_scale, rv, static_cast<const uint4*>(q), q_pos, n_q, out,
-        out_f32);
+        maps.k_codes, maps.v_codes, maps.k_scale, maps.v_scale, rv, qb, q_pos, n_q, out, out_f32);
   return cudaGetLastError();
 }
 

@@ -16,8 +16,8 @@
 //   t    = S_j * s_k (per column);  logit*log2(e) = t * s_q * log2(e)/sqrt(D)
 //   online softmax in base 2: e = exp2(t*r - m + c), l += e, with a running
 //   row maximum m that is only raised (and O rescaled) when a tile's maximum
-//   exceeds it by more than 2^8, so e <= 2^8 * 2^c; each tile takes two
-//   passes over S (the maximum, then the weights)
+//   exceeds it by more than 2^8, so e <= 2^8 * 2^c; a thread loads its whole
+//   S row of the tile once and works on registers
 //   P    = e * s_v (per column) rounded to fp16, written over S_j in TMEM
 //   O   += P . Vcodes_j                    tcgen05 kind::f16 (A = P from TMEM)
 //   out  = (O_0 a_0 + O_1 a_1) / (l_0 a_0 + l_1 a_1),  a_i = exp2(m_i - max m)
@@ -26,15 +26,15 @@
 // within the accuracy that e4m3 weights would lose.  2^c is a per-head power of
 // two (cancelling between O and l) that keeps P within fp16 range.
 //
-// Warp roles (448 threads):
+// Warp roles (384 threads):
 //   warps 0-3   stream 0 softmax, thread r owns query row r (TMEM lane r)
 //   warps 4-7   stream 1 softmax, same rows; both groups first run the query
 //               prologue (RoPE + e4m3 of the 128 rows) and finally the merge,
 //               each for half of the output columns
-//   warps 8-11  the per-head fp16 range factor, then the per-tile widening
+//   warps 8-9   the per-head fp16 range factor, then the per-tile widening
 //               of V to fp16
-//   warp 12     TMA producer (K, V codes and their scales, 4 stages)
-//   warp 13     TMEM allocation and MMA issue
+//   warp 10     TMA producer (K, V codes and their scales, 4 stages)
+//   warp 11     TMEM allocation and MMA issue
 #include <cfloat>
 
 #include "common.cuh"
@@ -45,7 +45,10 @@ namespace kvring_dev {
 constexpr int BM = 128;           // query rows per block
 constexpr int BN = 128;           // slots per tile
 constexpr int NSTAGE = 4;         // fp8 K/V stages
-constexpr int ATT_THREADS = 448;
+constexpr int ATT_THREADS = 384;
+constexpr int CONV_THREADS = 64;
+constexpr int WARP_TMA = 10;
+constexpr int WARP_MMA = 11;
 constexpr int SOFT_THREADS = 256;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TM_S = 0;      // stream s: fp32 S / fp16 P at columns 128 s
@@ -219,25 +222,25 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
   if (tid == 0) {
     for (int i = 0; i < NSTAGE; ++i) {
       mbar_init(&kv_full[i], 1);
-      mbar_init(&kv_empty[i], 1 + 4 + 4);   // QK commit, 4 widening warps, 4 softmax warps
+      mbar_init(&kv_empty[i], 1 + 2 + 4);   // QK commit, 2 widening warps, 4 softmax warps
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&vh_full[i], 4);
+      mbar_init(&vh_full[i], 2);
       mbar_init(&p_full[i], 4);
       mbar_init(&pv_done[i], 1);
     }
-    mbar_init(q_full, 12);
+    mbar_init(q_full, 10);
     for (int i = 0; i < 4; ++i) mbar_init(&ml_xchg[i], 2);
     *abort_flag = 0;
     *maxsv_bits = 0;
     fence_mbar_init();
   }
-  if (warp == 13) {
+  if (warp == WARP_MMA) {
     tmem_alloc(tmem_slot, TMEM_COLS);
     tmem_relinquish();
   }
-  if (warp == 12 && lane == 0) {
+  if (warp == WARP_TMA && lane == 0) {
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
     tma_prefetch_desc(&tmSK);
@@ -294,33 +297,44 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       const float4* sk4 = reinterpret_cast<const float4*>(sm + LY::SK0 + st * BN * 4);
       const float4* sv4 = reinterpret_cast<const float4*>(sm + LY::SV0 + st * BN * 4);
       const int valid = min(BN, n_valid - seq.tile(g, j) * BN);
-      // Pass 1: the tile's row maximum of t = S * s_k.  If it exceeds the
-      // running maximum by more than 2^8 (always on the first tile), raise the
-      // maximum and rescale O.  Pass 2: the weights, whose fp16 P is written
-      // over the S columns this pass has already read.  The chunk loops are
-      // kept rolled: an unrolled body does not fit the instruction cache.
-      float mt = -INFINITY;
-#pragma unroll 1
-      for (int cb = 0; cb < 4; ++cb) {
-        uint32_t x[32];
-        tmem_ld32(s_addr + cb * 32, x);
-        tmem_wait_ld();
-        const float4* k4p = sk4 + cb * 8;
-        const int vc = valid - cb * 32;
+      // The whole row of the tile (128 columns) comes in with one wait, so the
+      // maximum and the weights run on registers with 32-way parallelism.
+      // If the tile maximum exceeds the running maximum by more than 2^8
+      // (always on the first tile), the maximum is raised and O rescaled.
+      // P (fp16 pairs, 64 columns) is then written over the S buffer.
+      float x[128];
+      tmem_ld32(s_addr + 0, *reinterpret_cast<uint32_t(*)[32]>(x + 0));
+      tmem_ld32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(x + 32));
+      tmem_ld32(s_addr + 64, *reinterpret_cast<uint32_t(*)[32]>(x + 64));
+      tmem_ld32(s_addr + 96, *reinterpret_cast<uint32_t(*)[32]>(x + 96));
+      tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 32; i += 4) {
-          const float4 k4 = k4p[i >> 2];
-          float2 t0 = mul2(make_float2(__uint_as_float(x[i]), __uint_as_float(x[i + 1])), make_float2(k4.x, k4.y));
-          float2 t1 = mul2(make_float2(__uint_as_float(x[i + 2]), __uint_as_float(x[i + 3])), make_float2(k4.z, k4.w));
-          if (vc < 32) {
-            if (i >= vc) t0.x = -INFINITY;
-            if (i + 1 >= vc) t0.y = -INFINITY;
-            if (i + 2 >= vc) t1.x = -INFINITY;
-            if (i + 3 >= vc) t1.y = -INFINITY;
-          }
-          mt = max3f(mt, t0.x, t0.y);
-          mt = max3f(mt, t1.x, t1.y);
-        }
+      for (int i = 0; i < 128; i += 4) {
+        const float4 k4 = sk4[i >> 2];
+        const float2 t0 = mul2(make_float2(x[i], x[i + 1]), make_float2(k4.x, k4.y));
+        const float2 t1 = mul2(make_float2(x[i + 2], x[i + 3]), make_float2(k4.z, k4.w));
+        x[i] = t0.x;
+        x[i + 1] = t0.y;
+        x[i + 2] = t1.x;
+        x[i + 3] = t1.y;
+      }
+      if (valid < BN) {
+#pragma unroll
+        for (int i = 0; i < 128; ++i)
+          if (i >= valid) x[i] = -INFINITY;
+      }
+      float mt;
+      {
+        float m[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) m[i] = max3f(x[i], x[i + 16], fmaxf(x[i + 32], x[i + 48]));
+#pragma unroll
+        for (int i = 0; i < 16; ++i) m[i] = max3f(m[i], fmaxf(x[i + 64], x[i + 80]), fmaxf(x[i + 96], x[i + 112]));
+#pragma unroll
+        for (int w = 8; w > 0; w >>= 1)
+#pragma unroll
+          for (int i = 0; i < w; ++i) m[i] = fmaxf(m[i], m[i + w]);
+        mt = m[0];
       }
       const float m_tile = mt * rq;
       const bool grow = (j == 0) || (m_tile > m_run + kLazyRescale);
@@ -350,39 +364,25 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         m_run = m_new;
       }
       const float2 moff = make_float2(log2cv - m_run, log2cv - m_run);
-#pragma unroll 1
-      for (int cb = 0; cb < 4; ++cb) {
-        uint32_t x[32];
-        tmem_ld32(s_addr + cb * 32, x);
-        tmem_wait_ld();
-        const float4* k4p = sk4 + cb * 8;
-        const float4* v4p = sv4 + cb * 8;
-        const int vc = valid - cb * 32;
-        uint32_t pk[16];
+      uint32_t pk[64];
+      float2 l2 = make_float2(0.0f, 0.0f);
 #pragma unroll
-        for (int i = 0; i < 32; i += 4) {
-          const float4 k4 = k4p[i >> 2];
-          const float4 v4 = v4p[i >> 2];
-          float2 t0 = mul2(make_float2(__uint_as_float(x[i]), __uint_as_float(x[i + 1])), make_float2(k4.x, k4.y));
-          float2 t1 = mul2(make_float2(__uint_as_float(x[i + 2]), __uint_as_float(x[i + 3])), make_float2(k4.z, k4.w));
-          t0 = fma2(t0, rq2, moff);
-          t1 = fma2(t1, rq2, moff);
-          float2 e0 = make_float2(ex2f(t0.x), ex2f(t0.y));
-          float2 e1 = make_float2(ex2f(t1.x), ex2f(t1.y));
-          if (vc < 32) {
-            if (i >= vc) e0.x = 0.0f;
-            if (i + 1 >= vc) e0.y = 0.0f;
-            if (i + 2 >= vc) e1.x = 0.0f;
-            if (i + 3 >= vc) e1.y = 0.0f;
-          }
-          lacc = add2(lacc, add2(e0, e1));
-          const float2 p0 = mul2(e0, make_float2(v4.x, v4.y));
-          const float2 p1 = mul2(e1, make_float2(v4.z, v4.w));
-          pk[i >> 1] = cvt_f16x2(p0.x, p0.y);
-          pk[(i >> 1) + 1] = cvt_f16x2(p1.x, p1.y);
-        }
-        tmem_st16(s_addr + cb * 16, pk);
+      for (int i = 0; i < 128; i += 4) {
+        const float4 v4 = sv4[i >> 2];
+        const float2 a0 = fma2(make_float2(x[i], x[i + 1]), rq2, moff);
+        const float2 a1 = fma2(make_float2(x[i + 2], x[i + 3]), rq2, moff);
+        const float2 e0 = make_float2(ex2f(a0.x), ex2f(a0.y));
+        const float2 e1 = make_float2(ex2f(a1.x), ex2f(a1.y));
+        lacc = add2(lacc, e0);
+        l2 = add2(l2, e1);
+        const float2 p0 = mul2(e0, make_float2(v4.x, v4.y));
+        const float2 p1 = mul2(e1, make_float2(v4.z, v4.w));
+        pk[i >> 1] = cvt_f16x2(p0.x, p0.y);
+        pk[(i >> 1) + 1] = cvt_f16x2(p1.x, p1.y);
       }
+      lacc = add2(lacc, l2);
+#pragma unroll
+      for (int cb = 0; cb < 4; ++cb) tmem_st16(s_addr + cb * 16, *reinterpret_cast<uint32_t(*)[16]>(pk + 16 * cb));
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
@@ -455,7 +455,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       }
     }
     tc_fence_before();
-  } else if (warp < 12) {
+  } else if (warp < WARP_TMA) {
     // ======================================================== range factor + V widening
     const int ct = tid - SOFT_THREADS;
     {
@@ -466,7 +466,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       const int n4 = n_valid >> 2;
       float mx = 0.0f;
 #pragma unroll 4
-      for (int i = ct; i < n4; i += 128) {
+      for (int i = ct; i < n4; i += CONV_THREADS) {
         const float4 v = __ldg(vs + i);
         mx = fmaxf(mx, fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
       }
@@ -474,7 +474,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
       if (lane == 0) atomicMax(maxsv_bits, __float_as_int(mx));
-      asm volatile("bar.sync 1, 128;" ::: "memory");
+      asm volatile("bar.sync 1, 64;" ::: "memory");
       if (ct == 0) {
         const float m = __int_as_float(*maxsv_bits);
         // weights reach 2^8 * 2^c; with c = 6 - floor(log2 max s_v) every
@@ -483,7 +483,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         c = c < -64 ? -64 : (c > 64 ? 64 : c);
         *cv_smem = (float)c;
       }
-      asm volatile("bar.sync 1, 128;" ::: "memory");
+      asm volatile("bar.sync 1, 64;" ::: "memory");
       __syncwarp();
       if (lane == 0) mbar_arrive(q_full);
     }
@@ -501,8 +501,8 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       // eight consecutive threads take the same chunk of eight consecutive
       // slots, so their 16-byte reads and writes fall in distinct bank groups
 #pragma unroll
-      for (int it = 0; it < BN * CH / 128; ++it) {
-        const int task = it * 128 + ct;
+      for (int it = 0; it < BN * CH / CONV_THREADS; ++it) {
+        const int task = it * CONV_THREADS + ct;
         const int sl = 8 * (task / (8 * CH)) + (task & 7);
         const int c = (task >> 3) % CH;
         const uint4 w = *reinterpret_cast<const uint4*>(vsrc + kmajor_chunk<D>(sl, c));
@@ -530,7 +530,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         mbar_arrive(&kv_empty[st]);
       }
     }
-  } else if (warp == 12) {
+  } else if (warp == WARP_TMA) {
     // ======================================================== TMA producer
     if (lane == 0) {
       for (int u = 0; u < seq.count(); ++u) {
@@ -597,7 +597,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
 
   __syncthreads();
   if (tid == 0 && *abort_flag) atomicOr(&rv.state[ST_ERR], DEVERR_TIMEOUT);
-  if (warp == 13) {
+  if (warp == WARP_MMA) {
     tc_fence_after();
     tmem_dealloc(tmem, TMEM_COLS);
   }

@@ -31,27 +31,19 @@ __device__ __forceinline__ unsigned row_group_mask() {
 // ---------------------------------------------------------------- ring_kv_write
 // Block = T tokens x {K, V} x H heads x L lanes (thread order: token, kv,
 // head, lane), so the threads of one (token, kv) cover that token's H*D bf16
-// contiguously.  The RoPE cos/sin of the block's tokens are gathered into
-// shared memory once and reused by every head.
+// contiguously.  A K thread reads the cos/sin of its own 8 pairs (the token's
+// table row is shared by all heads through L1); there is no block barrier.
 template <int L>
 __global__ void __launch_bounds__(1024) ring_kv_write_kernel(RingView rv, const uint4* __restrict__ k,
                                                              const uint4* __restrict__ v,
                                                              const int32_t* __restrict__ pos, int n_new, int T) {
-  extern __shared__ float2 cs_smem[];  // [T][D/2]
   constexpr int D = L * 16;
-  constexpr int NP = D / 2;
   const int H = rv.H;
   const int t0 = blockIdx.x * T;
   const int wp = rv.state[ST_WP];
 
-  bool bad = false;
-  for (int i = threadIdx.x; i < T * NP; i += blockDim.x) {
-    const int tok = t0 + i / NP;
-    if (tok < n_new) cs_smem[i] = rope_cs(rv, pos + (size_t)tok * rv.n_axes, i % NP, bad);
-  }
-  if (bad) atomicOr(&rv.state[ST_ERR], DEVERR_POS_RANGE);
-  __syncthreads();
-
+  // This thread's 32 bytes of K or V go out first: they depend on nothing
+  // below, and the table gather and the barrier would otherwise delay them.
   const int per_tok = 2 * H * L;
   const int tl = threadIdx.x / per_tok;
   const int rem = threadIdx.x - tl * per_tok;
@@ -59,20 +51,29 @@ __global__ void __launch_bounds__(1024) ring_kv_write_kernel(RingView rv, const 
   const int h = (rem / L) % H;
   const int lane = rem % L;
   const int tok = t0 + tl;
-  if (tok < n_new) {  // uniform over the L lanes of a row
+  uint4 a = make_uint4(0, 0, 0, 0), b = a;
+  if (tok < n_new) {
     const uint4* src = (kv ? v : k) + ((size_t)tok * H + h) * (D / 8) + lane * 2;
-    const uint4 a = __ldg(src);
-    const uint4 b = __ldg(src + 1);
+    a = __ldg(src);
+    b = __ldg(src + 1);
+  }
+
+  bool bad = false;
+  float2 cs[8];
+  if (kv == 0 && tok < n_new) {
+    const int32_t* pr = pos + (size_t)tok * rv.n_axes;
+#pragma unroll
+    for (int m = 0; m < 8; ++m) cs[m] = rope_cs(rv, pr, lane * 8 + m, bad);
+  }
+  if (bad) atomicOr(&rv.state[ST_ERR], DEVERR_POS_RANGE);
+
+  if (tok < n_new) {  // uniform over the L lanes of a row
     float x[16];
     bf16x8_to_f32(a, x);
     bf16x8_to_f32(b, x + 8);
     if (kv == 0) {
-      const float2* cs = cs_smem + tl * NP + lane * 8;
 #pragma unroll
-      for (int m = 0; m < 8; ++m) {
-        const float2 c = cs[m];
-        rope_pair(x[2 * m], x[2 * m + 1], c.x, c.y);
-      }
+      for (int m = 0; m < 8; ++m) rope_pair(x[2 * m], x[2 * m + 1], cs[m].x, cs[m].y);
     }
     float amax = 0.0f;
 #pragma unroll
@@ -110,6 +111,11 @@ __global__ void __launch_bounds__(1024) ring_kv_write_kernel(RingView rv, const 
 template <int L>
 __global__ void __launch_bounds__(256) delta_rerotate_kernel(RingView rv, DeltaTable dt) {
   constexpr int D = L * 16;
+  // the lanes of a warp read 8 different pairs at once: from shared memory,
+  // not from the parameter space (which would serialise them)
+  __shared__ float2 cs_s[64];
+  if (threadIdx.x < 64) cs_s[threadIdx.x] = dt.cs[threadIdx.x];
+  __syncthreads();
   const int n_valid = rv.state[ST_NVALID];
   const long long gt = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const long long row = gt / L;
@@ -129,7 +135,10 @@ __global__ void __launch_bounds__(256) delta_rerotate_kernel(RingView rv, DeltaT
 #pragma unroll
   for (int m = 0; m < 8; ++m) {
     const int pr = lane * 8 + m;
-    if (pr < dt.n_pairs) rope_pair(x[2 * m], x[2 * m + 1], dt.cs[pr].x, dt.cs[pr].y);
+    if (pr < dt.n_pairs) {
+      const float2 c = cs_s[pr];
+      rope_pair(x[2 * m], x[2 * m + 1], c.x, c.y);
+    }
   }
   float amax = 0.0f;
 #pragma unroll
@@ -180,8 +189,7 @@ static cudaError_t launch_write_t(const RingView& rv, const void* k, const void*
   if (T < 1) T = 1;
   const int threads = per_tok * T;
   const int blocks = (n_new + T - 1) / T;
-  const size_t smem = (size_t)T * (L * 8) * sizeof(float2);
-  ring_kv_write_kernel<L><<<blocks, threads, smem, st>>>(rv, static_cast<const uint4*>(k),
+  ring_kv_write_kernel<L><<<blocks, threads, 0, st>>>(rv, static_cast<const uint4*>(k),
                                                          static_cast<const uint4*>(v), pos, n_new, T);
   return cudaGetLastError();
 }

@@ -12,7 +12,9 @@ value      attention calls (= steps) per second over all ranks
 e2e        the same through the C-ABI calls with the inputs copied from pinned
            host memory and the output copied back inside every step
 roofline   fp8_ring_attn, achieved FLOP/s vs the dense FP8 tensor peak
-           (measured bf16 burst x 2, the nominal fp8/bf16 ratio)
+           (measured bf16 burst x 2, the nominal fp8/bf16 ratio); the time is
+           that of the whole attend call, query preparation included, so the
+           attention kernel's own rate is a little higher
 kernels    per-kernel average launch time and rate (HBM GB/s for write and
            rerotate against the measured copy bandwidth)
 cpu_baseline   the oracle on a bounded sample, extrapolated, on host cores
@@ -49,6 +51,9 @@ WORKLOAD = "single attention call at the paper's shape: 24 heads x 128, 5788-slo
 WRITE_BYTES = N * H * (6 * D + 8) + 4 * N * 1          # bf16 K,V in; e4m3 K,V + 2 fp32 scales out; positions
 REROT_BYTES = S * H * (2 * D + 8)                      # K codes + K scale, read and written
 ATTN_FLOPS = 4 * N * S * D * H                         # QK^T and PV
+# kernels per step: ring_kv_write, delta_rerotate, and the attend call's two
+# (query RoPE + e4m3, then fp8_ring_attn)
+KERNELS_PER_STEP = 4
 
 
 # ---------------------------------------------------------------- distributed helpers
@@ -241,6 +246,7 @@ def run_gpu(args, rank, world, local_rank):
         t = time_graph(g, reps) / (reps * R)
         rate = work / t / (1e9 if unit == "GB/s" else 1e12)
         kern[name] = {"us": round(t * 1e6, 3), "rate": round(rate, 2), "unit": unit, "work_per_launch": work}
+    kern["fp8_ring_attn"]["timed"] = "kvring_attend call: query prep kernel + attention kernel"
     pk = peaks()
     fp8_peak = 2.0 * pk["bf16_tflops"]
     for name in ("ring_kv_write", "delta_rerotate"):
@@ -443,7 +449,7 @@ def main():
                        "rings_cycled": args.rings,
                        "l2": f"cold by construction: {args.rings} rings x ~50 MB cycled (> 129 MB L2)",
                        "graphs": "steps replayed from CUDA graphs", "parallelism": f"replicas x{world}"},
-            "clocks": res["clocks"], "gpu_launches": 3 * args.steps,
+            "clocks": res["clocks"], "gpu_launches": KERNELS_PER_STEP * args.steps,
             "e2e": res["e2e"], "roofline": roof, "kernels": res["kernels"],
             "cpu_baseline": cpu,
         }

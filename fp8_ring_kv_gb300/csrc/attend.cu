@@ -1,9 +1,11 @@
-// fp8_ring_attn: n_q bf16 queries attend over every valid slot of the FP8 ring.
+// fp8_ring_attn: n_q queries attend over every valid slot of the FP8 ring.
 //
 // Runway Characters paper, §4.3 (K and V stored as float8_e4m3, the queries
 // quantised per call, attention reading the FP8 cache directly) and
 // Appendix G (each call reads all the cache's slots; no causal mask).
 //
+// The queries arrive rotated and e4m3-coded, with one scale per (query,
+// head), from the query preparation kernel (query scratch of the workspace).
 // One block per (tile of 128 queries, head).  The slots are visited in tiles
 // of 128 in storage order: attention is a sum over the valid slots, so the
 // ring's wrap needs no reordering, and slots >= n_valid are masked.  The
@@ -28,12 +30,12 @@
 //
 // Warp roles (384 threads):
 //   warps 0-3   stream 0 softmax, thread r owns query row r (TMEM lane r)
-//   warps 4-7   stream 1 softmax, same rows; both groups first run the query
-//               prologue (RoPE + e4m3 of the 128 rows) and finally the merge,
-//               each for half of the output columns
+//   warps 4-7   stream 1 softmax, same rows; both groups finally run the
+//               merge, each for half of the output columns
 //   warps 8-9   the per-head fp16 range factor, then the per-tile widening
 //               of V to fp16
-//   warp 10     TMA producer (K, V codes and their scales, 4 stages)
+//   warp 10     TMA producer (the e4m3 query tile, then K, V codes and their
+//               scales, 4 stages)
 //   warp 11     TMEM allocation and MMA issue
 #include <cfloat>
 
@@ -112,82 +114,12 @@ struct TileSeq {
   __device__ int tile(int s, int j) const { return s * T0 + j; }
 };
 
-// Query rows [r0, r0 + 16) by one warp: lane l owns channels [l*C, l*C + C)
-// (C = D/32), loads are coalesced along the row; RoPE in fp32, the row's
-// absmax by shuffles, e4m3 codes into the K-major Q tile.
-template <int D>
-__device__ __forceinline__ void query_rows(const RingView& rv, const __nv_bfloat16* __restrict__ q,
-                                           const int32_t* __restrict__ q_pos, int n_q, int h, int qt, int r0,
-                                           uint8_t* qtile, float* sq_smem, bool& bad) {
-  constexpr int C = D / 32;     // channels per lane: 4 or 2
-  constexpr int PP = C / 2;     // pairs per lane
-  constexpr int R = 8;          // rows in flight per batch
-  const int lane = threadIdx.x & 31;
-  const int H = rv.H;
-#pragma unroll 1
-  for (int r1 = r0; r1 < r0 + 16; r1 += R) {
-    float x[R][C];
-    float2 cs[R][PP];
-#pragma unroll
-    for (int i = 0; i < R; ++i) {
-      const int qi = qt * BM + r1 + i;
-      if (qi < n_q) {
-        const __nv_bfloat16* src = q + ((size_t)qi * H + h) * D + lane * C;
-        if constexpr (C == 4) {
-          const uint2 u = __ldg(reinterpret_cast<const uint2*>(src));
-          x[i][0] = __uint_as_float(u.x << 16);
-          x[i][1] = __uint_as_float(u.x & 0xFFFF0000u);
-          x[i][2] = __uint_as_float(u.y << 16);
-          x[i][3] = __uint_as_float(u.y & 0xFFFF0000u);
-        } else {
-          const uint32_t u = __ldg(reinterpret_cast<const uint32_t*>(src));
-          x[i][0] = __uint_as_float(u << 16);
-          x[i][1] = __uint_as_float(u & 0xFFFF0000u);
-        }
-        const int32_t* pr = q_pos + (size_t)qi * rv.n_axes;
-#pragma unroll
-        for (int m = 0; m < PP; ++m) cs[i][m] = rope_cs(rv, pr, lane * PP + m, bad);
-      } else {
-#pragma unroll
-        for (int m = 0; m < C; ++m) x[i][m] = 0.0f;
-#pragma unroll
-        for (int m = 0; m < PP; ++m) cs[i][m] = make_float2(1.0f, 0.0f);
-      }
-    }
-#pragma unroll
-    for (int i = 0; i < R; ++i) {
-      const int r = r1 + i;
-#pragma unroll
-      for (int m = 0; m < PP; ++m) rope_pair(x[i][2 * m], x[i][2 * m + 1], cs[i][m].x, cs[i][m].y);
-      float amax = 0.0f;
-#pragma unroll
-      for (int m = 0; m < C; ++m) amax = fmaxf(amax, fabsf(x[i][m]));
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
-      float scale, inv;
-      absmax_scale(amax, scale, inv);
-      uint32_t codes = 0;
-      if (inv != 0.0f) {
-        codes = cvt_e4m3x2(__fmul_rn(x[i][0], inv), __fmul_rn(x[i][1], inv));
-        if constexpr (C == 4) codes |= (uint32_t)cvt_e4m3x2(__fmul_rn(x[i][2], inv), __fmul_rn(x[i][3], inv)) << 16;
-      }
-      const int byte = lane * C;   // channel offset = byte offset of the codes
-      uint8_t* dst = qtile + kmajor_chunk<D>(r, byte >> 4) + (byte & 15);
-      if constexpr (C == 4)
-        *reinterpret_cast<uint32_t*>(dst) = codes;
-      else
-        *reinterpret_cast<uint16_t*>(dst) = (uint16_t)codes;
-      if (lane == 0) sq_smem[r] = scale;
-    }
-  }
-}
-
 template <int D>
 __global__ void __launch_bounds__(ATT_THREADS, 1)
     fp8_ring_attn_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                          const __grid_constant__ CUtensorMap tmSK, const __grid_constant__ CUtensorMap tmSV,
-                         RingView rv, const __nv_bfloat16* __restrict__ q, const int32_t* __restrict__ q_pos,
-                         int n_q, void* __restrict__ out, int out_f32) {
+                         const __grid_constant__ CUtensorMap tmQ, RingView rv, int n_q, void* __restrict__ out,
+                         int out_f32) {
   using LY = AttnLayout<D>;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned base, derived by offsetting the __shared__ array itself
@@ -206,7 +138,6 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + LY::MISC + 4);
   int* maxsv_bits = reinterpret_cast<int*>(sm + LY::MISC + 8);
   float* cv_smem = reinterpret_cast<float*>(sm + LY::MISC + 12);   // log2 of the per-head weight factor
-  float* sq_smem = reinterpret_cast<float*>(sm + LY::SQ);
   float* ml = reinterpret_cast<float*>(sm + LY::ML);
 
   const int tid = threadIdx.x;
@@ -230,7 +161,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       mbar_init(&p_full[i], 4);
       mbar_init(&pv_done[i], 1);
     }
-    mbar_init(q_full, 10);
+    mbar_init(q_full, 1 + 2);   // the query tile's TMA, 2 widening warps (range factor)
     for (int i = 0; i < 4; ++i) mbar_init(&ml_xchg[i], 2);
     *abort_flag = 0;
     *maxsv_bits = 0;
@@ -245,6 +176,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
     tma_prefetch_desc(&tmV);
     tma_prefetch_desc(&tmSK);
     tma_prefetch_desc(&tmSV);
+    tma_prefetch_desc(&tmQ);
   }
   __syncthreads();
   tc_fence_after();
@@ -262,15 +194,6 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
     }
     if (tid == 0 && qt == 0 && h == 0) atomicOr(&rv.state[ST_ERR], DEVERR_EMPTY);
   } else if (warp < 8) {
-    // ======================================================== query prologue
-    {
-      bool bad = false;
-      query_rows<D>(rv, q, q_pos, n_q, h, qt, warp * 16, sm + LY::Q, sq_smem, bad);
-      if (bad) atomicOr(&rv.state[ST_ERR], DEVERR_POS_RANGE);
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(q_full);
-    }
     // ======================================================== softmax of stream g
     const int g = warp >> 2;
     const int r = tid & 127;                     // query row = TMEM lane
@@ -278,8 +201,9 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
     const uint32_t s_addr = tmem + lane_off + TM_S + g * 128;
     const uint32_t o_addr = tmem + lane_off + TM_O + g * 128;
     constexpr float kRowC = (D == 128 ? 0.08838834764831845f : 0.125f) * 1.4426950408889634f;
+    const int qrow = qt * BM + r;
+    const float sq = qrow < n_q ? rv.q_scale[(size_t)h * rv.Q_pad + qrow] : 0.0f;
     bool ok = mbar_wait(q_full, 0, abort_flag);
-    const float sq = sq_smem[r];
     const float rq = sq > 0.0f ? sq * kRowC : 1.0f;
     const float log2cv = *cv_smem;
     const float2 rq2 = make_float2(rq, rq);
@@ -533,6 +457,8 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
   } else if (warp == WARP_TMA) {
     // ======================================================== TMA producer
     if (lane == 0) {
+      mbar_arrive_expect_tx(q_full, BM * D);
+      tma_load_3d(sm + LY::Q, &tmQ, q_full, 0, h, qt * BM);
       for (int u = 0; u < seq.count(); ++u) {
         int sg, j;
         seq.at(u, sg, j);
@@ -611,16 +537,15 @@ cudaError_t prepare_attend(int D) {
                               AttnLayout<64>::ALLOC);
 }
 
-cudaError_t launch_fp8_ring_attn(const RingView& rv, const AttnMaps& maps, const void* q, const int32_t* q_pos,
-                                 int n_q, void* out, int out_f32, cudaStream_t st) {
+cudaError_t launch_fp8_ring_attn(const RingView& rv, const AttnMaps& maps, const CUtensorMap& tmQ, int n_q, void* out,
+                                 int out_f32, cudaStream_t st) {
   const dim3 grid((n_q + BM - 1) / BM, rv.H);
-  const __nv_bfloat16* qb = static_cast<const __nv_bfloat16*>(q);
   if (rv.D == 128)
     fp8_ring_attn_kernel<128><<<grid, ATT_THREADS, AttnLayout<128>::ALLOC, st>>>(
-        maps.k_codes, maps.v_codes, maps.k_scale, maps.v_scale, rv, qb, q_pos, n_q, out, out_f32);
+        maps.k_codes, maps.v_codes, maps.k_scale, maps.v_scale, tmQ, rv, n_q, out, out_f32);
   else
     fp8_ring_attn_kernel<64><<<grid, ATT_THREADS, AttnLayout<64>::ALLOC, st>>>(
-        maps.k_codes, maps.v_codes, maps.k_scale, maps.v_scale, rv, qb, q_pos, n_q, out, out_f32);
+        maps.k_codes, maps.v_codes, maps.k_scale, maps.v_scale, tmQ, rv, n_q, out, out_f32);
   return cudaGetLastError();
 }
 

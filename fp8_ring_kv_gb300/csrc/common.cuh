@@ -28,7 +28,9 @@ struct RingView {
   uint8_t* v_codes;               // [H][S][D]
   float* k_scale;                 // [H][S_pad]
   float* v_scale;                 // [H][S_pad]
-  int32_t H, D, S, S_pad, n_axes;
+  uint8_t* q_codes;               // query scratch: e4m3 [n_q][H][D]
+  float* q_scale;                 // query scratch: fp32 [H][Q_pad]
+  int32_t H, D, S, S_pad, n_axes, Q_pad;
 };
 
 // ---------------------------------------------------------------- numerics

@@ -19,6 +19,7 @@ struct kvring {
   kvring_config cfg;
   RingView rv;
   AttnMaps maps;
+  CUtensorMap q_map;  // e4m3 query scratch, [max_queries][H][D]
   int device;
 };
 
@@ -36,8 +37,8 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct Layout {
-  size_t state, rope[3], k_codes, v_codes, k_scale, v_scale, total;
-  int s_pad;
+  size_t state, rope[3], k_codes, v_codes, k_scale, v_scale, q_codes, q_scale, total;
+  int s_pad, q_pad;
 };
 
 bool check_config(const kvring_config* c) {
@@ -55,6 +56,7 @@ bool check_config(const kvring_config* c) {
   if (sum != c->head_dim) return false;
   if (!(c->rope_base > 1.0) || !std::isfinite(c->rope_base)) return false;
   if (c->out_dtype != KVRING_OUT_BF16 && c->out_dtype != KVRING_OUT_F32) return false;
+  if (c->max_queries < 1 || c->max_queries > (1 << 20)) return false;
   return true;
 }
 
@@ -77,6 +79,11 @@ Layout layout_of(const kvring_config* c) {
   off = round_up(off + H * L.s_pad * sizeof(float), 1024);
   L.v_scale = off;
   off = round_up(off + H * L.s_pad * sizeof(float), 1024);
+  L.q_pad = (int)round_up(c->max_queries, 4);
+  L.q_codes = off;
+  off = round_up(off + (size_t)c->max_queries * H * D, 1024);
+  L.q_scale = off;
+  off = round_up(off + H * L.q_pad * sizeof(float), 1024);
   L.total = off;
   return L;
 }
@@ -97,12 +104,28 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
+// Query codes [n_rows][H][D] at q_codes: box of D channels x 1 head x 128
+// queries, swizzled like the key tiles (rows beyond n_rows read as zero).
+bool encode_query_map(CUtensorMap* m, const void* q_codes, int H, int D, int n_rows) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)n_rows};
+  const cuuint64_t strides[2] = {(cuuint64_t)D, (cuuint64_t)H * D};
+  const cuuint32_t box[3] = {(cuuint32_t)D, 1, 128};
+  const cuuint32_t es[3] = {1, 1, 1};
+  const CUtensorMapSwizzle sw = D == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(q_codes), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool encode_maps(kvring* r) {
   auto enc = tensor_map_encoder();
   if (!enc) return false;
   const RingView& rv = r->rv;
   const cuuint64_t D = rv.D, S = rv.S, H = rv.H;
   const CUtensorMapSwizzle sw = rv.D == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  if (!encode_query_map(&r->q_map, rv.q_codes, rv.H, rv.D, r->cfg.max_queries)) return false;
   {
     const cuuint64_t dims[3] = {D, S, H};
     const cuuint64_t strides[2] = {D, S * D};
@@ -182,6 +205,9 @@ int kvring_create(const kvring_config* cfg, void* workspace, size_t workspace_by
   rv.v_codes = ws + L.v_codes;
   rv.k_scale = reinterpret_cast<float*>(ws + L.k_scale);
   rv.v_scale = reinterpret_cast<float*>(ws + L.v_scale);
+  rv.q_codes = ws + L.q_codes;
+  rv.q_scale = reinterpret_cast<float*>(ws + L.q_scale);
+  rv.Q_pad = L.q_pad;
   rv.H = cfg->heads;
   rv.D = cfg->head_dim;
   rv.S = cfg->n_slots;
@@ -189,7 +215,7 @@ int kvring_create(const kvring_config* cfg, void* workspace, size_t workspace_by
   rv.n_axes = cfg->n_axes;
 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  // state, codes and scales start at zero: an empty ring
+  // state, codes and scales (and the query scratch) start at zero: an empty ring
   if ((e = cudaMemsetAsync(ws + L.state, 0, L.rope[0] - L.state, st)) != cudaSuccess ||
       (e = cudaMemsetAsync(ws + L.k_codes, 0, L.total - L.k_codes, st)) != cudaSuccess) {
     delete r;
@@ -249,11 +275,12 @@ int kvring_reset_positions(kvring* r, int32_t d, kvring_stream stream) {
 
 int kvring_attend(kvring* r, const void* q, const int32_t* q_pos, int32_t n_q, void* out, kvring_stream stream) {
   if (!r || !q || !q_pos || !out) return KVRING_ERR_INVALID_ARG;
-  if (n_q < 1) return KVRING_ERR_INVALID_ARG;
+  if (n_q < 1 || n_q > r->cfg.max_queries) return KVRING_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(out, 16) || !aligned(q_pos, 4)) return KVRING_ERR_MISALIGNED;
-  const cudaError_t e = launch_fp8_ring_attn(r->rv, r->maps, q, q_pos, n_q, out,
-                                             r->cfg.out_dtype == KVRING_OUT_F32,
-                                             reinterpret_cast<cudaStream_t>(stream));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_q_prep(r->rv, q, q_pos, n_q, st);
+  if (e == cudaSuccess)
+    e = launch_fp8_ring_attn(r->rv, r->maps, r->q_map, n_q, out, r->cfg.out_dtype == KVRING_OUT_F32, st);
   return e == cudaSuccess ? KVRING_OK : cuda_fail(e);
 }
 

@@ -26,8 +26,10 @@ cudaError_t launch_ring_kv_write(const RingView& rv, const void* k, const void* 
 cudaError_t launch_delta_rerotate(const RingView& rv, const DeltaTable& dt, cudaStream_t st);
 cudaError_t launch_debug_quantize(const float* x, long long rows, int d, uint8_t* codes, float* scales,
                                   cudaStream_t st);
+cudaError_t launch_q_prep(const RingView& rv, const void* q, const int32_t* q_pos, int n_q, cudaStream_t st);
 cudaError_t prepare_attend(int D);   // once per device: opt in to the kernel's shared memory
-cudaError_t launch_fp8_ring_attn(const RingView& rv, const AttnMaps& maps, const void* q, const int32_t* q_pos,
-                                 int n_q, void* out, int out_f32, cudaStream_t st);
+// tmQ: the query codes of this call (rv.q_codes), [n_q][H][D] u8, box {D, 1, 128}
+cudaError_t launch_fp8_ring_attn(const RingView& rv, const AttnMaps& maps, const CUtensorMap& tmQ, int n_q, void* out,
+                                 int out_f32, cudaStream_t st);
 
 }  // namespace kvring_dev

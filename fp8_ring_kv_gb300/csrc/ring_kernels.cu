@@ -103,6 +103,46 @@ __global__ void __launch_bounds__(1024) ring_kv_write_kernel(RingView rv, const 
   }
 }
 
+// ---------------------------------------------------------------- query preparation
+// The queries of one attention call: RoPE in fp32 at their positions and
+// e4m3 with one absmax scale per (query, head), into the workspace's query
+// scratch (codes [n_q][H][D], scales [H][Q_pad]) that the attention kernel
+// then loads by TMA.  Same thread layout and arithmetic as the K side of
+// ring_kv_write.
+template <int L>
+__global__ void __launch_bounds__(256) q_prep_kernel(RingView rv, const uint4* __restrict__ q,
+                                                     const int32_t* __restrict__ pos, int n_q) {
+  constexpr int D = L * 16;
+  const long long gt = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const long long row = gt / L;            // = query * H + head
+  const int lane = (int)(gt % L);
+  if (row >= (long long)n_q * rv.H) return;  // whole rows
+  const int qi = (int)(row / rv.H);
+  const int h = (int)(row % rv.H);
+  const uint4* src = q + row * (D / 8) + lane * 2;
+  const uint4 a = __ldg(src);
+  const uint4 b = __ldg(src + 1);
+  bool bad = false;
+  float2 cs[8];
+  const int32_t* pr = pos + (size_t)qi * rv.n_axes;
+#pragma unroll
+  for (int m = 0; m < 8; ++m) cs[m] = rope_cs(rv, pr, lane * 8 + m, bad);
+  if (bad) atomicOr(&rv.state[ST_ERR], DEVERR_POS_RANGE);
+  float x[16];
+  bf16x8_to_f32(a, x);
+  bf16x8_to_f32(b, x + 8);
+#pragma unroll
+  for (int m = 0; m < 8; ++m) rope_pair(x[2 * m], x[2 * m + 1], cs[m].x, cs[m].y);
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
+  amax = row_max<L>(amax, __activemask() & row_group_mask<L>());
+  float scale, inv;
+  absmax_scale(amax, scale, inv);
+  *reinterpret_cast<uint4*>(rv.q_codes + row * D + lane * 16) = quant16(x, inv);
+  if (lane == 0) rv.q_scale[(size_t)h * rv.Q_pad + qi] = scale;
+}
+
 // ---------------------------------------------------------------- delta_rerotate
 // One thread per 16 codes of a key row, over rows (head, slot) with
 // slot < n_valid.  In place: dequantise (code * scale, fp32), rotate the
@@ -198,6 +238,17 @@ cudaError_t launch_ring_kv_write(const RingView& rv, const void* k, const void* 
                                  cudaStream_t st) {
   if (rv.D == 64) return launch_write_t<4>(rv, k, v, pos, n_new, st);
   return launch_write_t<8>(rv, k, v, pos, n_new, st);
+}
+
+cudaError_t launch_q_prep(const RingView& rv, const void* q, const int32_t* q_pos, int n_q, cudaStream_t st) {
+  const int L = rv.D / 16;
+  const long long threads = (long long)n_q * rv.H * L;
+  const unsigned blocks = (unsigned)((threads + 255) / 256);
+  if (L == 4)
+    q_prep_kernel<4><<<blocks, 256, 0, st>>>(rv, static_cast<const uint4*>(q), q_pos, n_q);
+  else
+    q_prep_kernel<8><<<blocks, 256, 0, st>>>(rv, static_cast<const uint4*>(q), q_pos, n_q);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_delta_rerotate(const RingView& rv, const DeltaTable& dt, cudaStream_t st) {

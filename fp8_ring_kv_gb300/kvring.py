@@ -46,6 +46,7 @@ class kvring_config(ctypes.Structure):
         ("pos_count", ctypes.c_int32 * 3),
         ("rope_base", ctypes.c_double),
         ("out_dtype", ctypes.c_int32),
+        ("max_queries", ctypes.c_int32),
     ]
 
 
@@ -108,7 +109,8 @@ def _ptr(t) -> ctypes.c_void_p:
 
 
 def make_config(heads, head_dim, n_slots, axis_dims, pos_min, pos_count, rope_base=10000.0,
-                out_dtype=KVRING_OUT_F32) -> kvring_config:
+                out_dtype=KVRING_OUT_F32, max_queries=None) -> kvring_config:
+    """max_queries defaults to n_slots (a call attends at most one ring's worth of queries)."""
     c = kvring_config()
     c.heads, c.head_dim, c.n_slots = int(heads), int(head_dim), int(n_slots)
     c.n_axes = len(axis_dims)
@@ -118,6 +120,7 @@ def make_config(heads, head_dim, n_slots, axis_dims, pos_min, pos_count, rope_ba
         c.pos_count[a] = int(pos_count[a]) if a < len(axis_dims) else 0
     c.rope_base = float(rope_base)
     c.out_dtype = int(out_dtype)
+    c.max_queries = int(n_slots if max_queries is None else max_queries)
     return c
 
 
@@ -163,8 +166,9 @@ class KVRing:
     the current (or given) stream and return at once."""
 
     def __init__(self, heads, head_dim, n_slots, axis_dims, pos_min, pos_count, rope_base=10000.0,
-                 out_dtype=KVRING_OUT_F32, device="cuda", stream=None):
-        self.cfg = make_config(heads, head_dim, n_slots, axis_dims, pos_min, pos_count, rope_base, out_dtype)
+                 out_dtype=KVRING_OUT_F32, device="cuda", stream=None, max_queries=None):
+        self.cfg = make_config(heads, head_dim, n_slots, axis_dims, pos_min, pos_count, rope_base, out_dtype,
+                               max_queries)
         nbytes = kvring_workspace_bytes(self.cfg)
         if nbytes == 0:
             raise KVRingError("invalid kvring configuration")
@@ -189,9 +193,9 @@ class KVRing:
         self.state_words = ws[off[4]:off[4] + 16].view(torch.int32)
 
     @classmethod
-    def from_shape(cls, shape, out_dtype=KVRING_OUT_F32, device="cuda", stream=None):
+    def from_shape(cls, shape, out_dtype=KVRING_OUT_F32, device="cuda", stream=None, max_queries=None):
         return cls(shape.heads, shape.head_dim, shape.n_slots, shape.axis_dims, shape.pos_min, shape.pos_count,
-                   shape.rope_base, out_dtype, device, stream)
+                   shape.rope_base, out_dtype, device, stream, max_queries)
 
     def write(self, k, v, pos, stream=None):
         kvring_write(self.handle, k, v, pos, k.shape[0], stream)

@@ -86,6 +86,11 @@ enum { KVRING_OUT_BF16 = 0, KVRING_OUT_F32 = 1 };
  *              (KVRING_DEVERR_POS_RANGE)
  *   rope_base  the frequency base: omega_{a,j} = rope_base^(-2j/axis_dims[a])
  *   out_dtype  KVRING_OUT_BF16 or KVRING_OUT_F32 for kvring_attend's output
+ *   max_queries  the largest n_q one kvring_attend call may pass, 1 .. 1<<20;
+ *              the workspace holds that many rotated, e4m3-coded query rows
+ *              (max_queries * H * D bytes + their fp32 scales) as per-call
+ *              scratch, so two kvring_attend calls on one ring must not run
+ *              at the same time (in stream order they may follow each other)
  */
 typedef struct {
   int32_t heads;
@@ -97,6 +102,7 @@ typedef struct {
   int32_t pos_count[3];
   double rope_base;
   int32_t out_dtype;
+  int32_t max_queries;
 } kvring_config;
 
 /* Bytes of device workspace kvring_create needs for this configuration
@@ -149,10 +155,11 @@ int kvring_reset_positions(kvring* r, int32_t d, kvring_stream stream);
  * scales) and App. G (all slots read).
  *   q      device bf16 [n_q][H][D], 16-byte aligned
  *   q_pos  device int32 [n_q][n_axes]
- *   n_q    >= 1
+ *   n_q    1 .. max_queries
  *   out    device [n_q][H][D], bf16 or fp32 as configured, 16-byte aligned
  * Each query row is rotated by RoPE at q_pos (fp32) and quantised to e4m3
- * with its own scale; out = softmax(q.k / sqrt(D)) v over slots
+ * with its own scale (a first kernel writes these codes to the workspace's
+ * query scratch); out = softmax(q.k / sqrt(D)) v over slots
  * 0 .. n_valid-1 with dequantised q, k and v, no mask.  Scores come from FP8
  * tensor-core products with fp32 accumulation; the softmax weights are
  * rounded to fp16 for the weighted sum of V.

@@ -1,0 +1,143 @@
+"""The C ABI without a GPU: the library loads, exports every function that
+include/*.h declares, and rejects bad arguments on the host before it makes
+any CUDA call.  No call here reaches a kernel or a CUDA API."""
+import ctypes
+import glob
+import math
+import os
+import re
+
+import pytest
+
+from fp8_ring_kv_gb300 import kvring as K
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADERS = sorted(glob.glob(os.path.join(ROOT, "include", "*.h")))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(K.LIB_PATH):
+        from fp8_ring_kv_gb300 import build
+        build.build()
+    return K.load()
+
+
+def declared_functions():
+    names = set()
+    for h in HEADERS:
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        text = re.sub(r"#[^\n]*", " ", text)
+        names.update(re.findall(r"\b(kvring_[a-z0-9_]+)\s*\(", text))
+    return sorted(names)
+
+
+def paper_config(**kw):
+    c = K.make_config(24, 128, 5788, (32, 48, 48), (-40000, 0, 0), (80000, 64, 64))
+    for k, v in kw.items():
+        setattr(c, k, v)
+    return c
+
+
+def test_header_declares_the_calls():
+    names = declared_functions()
+    for must in ("kvring_create", "kvring_write", "kvring_reset_positions", "kvring_attend", "kvring_destroy",
+                 "kvring_workspace_bytes"):
+        assert must in names
+
+
+def test_every_declared_function_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in include/ but not exported by libkvring.so"
+
+
+def test_binding_uses_the_same_names(lib):
+    for name in declared_functions():
+        fn = getattr(lib, name)
+        assert fn.argtypes is not None, f"{name} has no ctypes signature in the binding"
+
+
+def test_workspace_bytes_valid_configuration(lib):
+    c = paper_config()
+    n = K.kvring_workspace_bytes(c)
+    H, D, S = 24, 128, 5788
+    # at least the two code arrays, the two scale arrays and the query scratch
+    assert n >= 2 * H * S * D + 2 * H * S * 4 + S * H * D
+    assert n % 1024 == 0
+    # grows with the ring and with the query scratch
+    assert K.kvring_workspace_bytes(paper_config(n_slots=S + 1000)) > n
+    assert K.kvring_workspace_bytes(paper_config(max_queries=2 * S)) > n
+    assert K.kvring_workspace_bytes(paper_config(max_queries=1)) < n
+
+
+@pytest.mark.parametrize("field,value", [
+    ("head_dim", 96), ("head_dim", 256), ("heads", 0), ("n_slots", 0), ("n_slots", (1 << 20) + 1),
+    ("n_axes", 0), ("n_axes", 4), ("rope_base", 1.0), ("rope_base", math.nan), ("rope_base", math.inf),
+    ("out_dtype", 7), ("max_queries", 0), ("max_queries", (1 << 20) + 1),
+])
+def test_workspace_bytes_rejects_invalid(lib, field, value):
+    assert K.kvring_workspace_bytes(paper_config(**{field: value})) == 0
+
+
+def test_workspace_bytes_rejects_bad_axes(lib):
+    c = paper_config()
+    c.axis_dims[0] = 30                       # axes no longer sum to head_dim
+    assert K.kvring_workspace_bytes(c) == 0
+    c = paper_config()
+    c.axis_dims[1], c.axis_dims[2] = 47, 49   # odd axis
+    assert K.kvring_workspace_bytes(c) == 0
+    c = paper_config()
+    c.pos_count[0] = 0
+    assert K.kvring_workspace_bytes(c) == 0
+
+
+def test_status_strings(lib):
+    codes = [K.KVRING_OK, K.KVRING_ERR_INVALID_ARG, K.KVRING_ERR_MISALIGNED, K.KVRING_ERR_UNSUPPORTED,
+             K.KVRING_ERR_CUDA, K.KVRING_ERR_WORKSPACE, K.KVRING_ERR_NO_DEVICE]
+    texts = [lib.kvring_status_string(c).decode() for c in codes]
+    assert len(set(texts)) == len(texts) and all(texts)
+    assert lib.kvring_status_string(12345).decode() == "unknown status"
+
+
+def _vp(x):
+    return ctypes.c_void_p(x)
+
+
+def test_create_rejects_before_any_cuda_call(lib):
+    c = paper_config()
+    need = K.kvring_workspace_bytes(c)
+    h = ctypes.c_void_p()
+    # the fake workspace addresses are never dereferenced: each case fails a host check first
+    assert lib.kvring_create(None, _vp(1 << 20), need, None, ctypes.byref(h)) == K.KVRING_ERR_INVALID_ARG
+    assert lib.kvring_create(ctypes.byref(c), None, need, None, ctypes.byref(h)) == K.KVRING_ERR_INVALID_ARG
+    assert lib.kvring_create(ctypes.byref(c), _vp((1 << 20) + 16), need, None, ctypes.byref(h)) \
+        == K.KVRING_ERR_MISALIGNED
+    assert lib.kvring_create(ctypes.byref(c), _vp(1 << 20), need - 1, None, ctypes.byref(h)) \
+        == K.KVRING_ERR_WORKSPACE
+    assert h.value is None
+    bad = paper_config(head_dim=96)
+    assert lib.kvring_create(ctypes.byref(bad), _vp(1 << 20), need, None, ctypes.byref(h)) \
+        == K.KVRING_ERR_INVALID_ARG
+    assert lib.kvring_create(ctypes.byref(c), _vp(1 << 20), need, None, None) == K.KVRING_ERR_INVALID_ARG
+
+
+def test_calls_on_null_handle(lib):
+    p = _vp(1 << 20)
+    assert lib.kvring_write(None, p, p, p, 1, None) == K.KVRING_ERR_INVALID_ARG
+    assert lib.kvring_reset_positions(None, 5, None) == K.KVRING_ERR_INVALID_ARG
+    assert lib.kvring_attend(None, p, p, 1, p, None) == K.KVRING_ERR_INVALID_ARG
+    assert lib.kvring_destroy(None) == K.KVRING_OK
+    out3 = (ctypes.c_int32 * 3)()
+    assert lib.kvring_debug_state(None, None, out3) == K.KVRING_ERR_INVALID_ARG
+    assert lib.kvring_layout(None, None, None, None, None, None, None) == K.KVRING_ERR_INVALID_ARG
+
+
+def test_debug_quantize_host_checks(lib):
+    p = _vp(1 << 20)
+    assert lib.kvring_debug_quantize(None, 4, 128, p, p, None) == K.KVRING_ERR_INVALID_ARG
+    assert lib.kvring_debug_quantize(p, 0, 128, p, p, None) == K.KVRING_ERR_INVALID_ARG
+    assert lib.kvring_debug_quantize(p, 4, 48, p, p, None) == K.KVRING_ERR_UNSUPPORTED
+    assert lib.kvring_debug_quantize(_vp((1 << 20) + 4), 4, 128, p, p, None) == K.KVRING_ERR_MISALIGNED
+    assert lib.kvring_debug_quantize(p, 4, 128, p, _vp((1 << 20) + 2), None) == K.KVRING_ERR_MISALIGNED

@@ -1,8 +1,10 @@
 // Host side of libkvring: argument checks, workspace layout, RoPE tables,
 // TMA descriptors and kernel launches.  See include/kvring.h for the contract.
+#include <atomic>
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <vector>
 
@@ -14,6 +16,11 @@
 #include "launch.h"
 
 using namespace kvring_dev;
+
+// Query scratch of kvring_attend_noalloc: one array per device, part of the
+// library's device image (no allocation at run time).  Nothing in it has to
+// start at zero.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[KVRING_NOALLOC_SCRATCH_BYTES];
 
 struct kvring {
   kvring_config cfg;
@@ -157,6 +164,30 @@ bool encode_maps(kvring* r) {
   return true;
 }
 
+// Device address of g_noalloc_scratch, looked up once per device with that
+// device current.
+constexpr int kNoallocDevices = 64;
+std::atomic<uint8_t*> g_noalloc_addr[kNoallocDevices];
+std::mutex g_noalloc_setup;
+
+int noalloc_scratch(int dev, uint8_t** out) {
+  if (dev < 0 || dev >= kNoallocDevices) return KVRING_ERR_UNSUPPORTED;
+  uint8_t* p = g_noalloc_addr[dev].load(std::memory_order_acquire);
+  if (!p) {
+    std::lock_guard<std::mutex> lock(g_noalloc_setup);
+    p = g_noalloc_addr[dev].load(std::memory_order_relaxed);
+    if (!p) {
+      void* a = nullptr;
+      const cudaError_t e = cudaGetSymbolAddress(&a, g_noalloc_scratch);
+      if (e != cudaSuccess) return cuda_fail(e);
+      p = static_cast<uint8_t*>(a);
+      g_noalloc_addr[dev].store(p, std::memory_order_release);
+    }
+  }
+  *out = p;
+  return KVRING_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -284,6 +315,36 @@ int kvring_attend(kvring* r, const void* q, const int32_t* q_pos, int32_t n_q, v
   return e == cudaSuccess ? KVRING_OK : cuda_fail(e);
 }
 
+int kvring_attend_noalloc(kvring* r, const void* q, const int32_t* q_pos, int32_t n_q, void* out,
+                          kvring_stream stream) {
+  if (!r || !q || !q_pos || !out) return KVRING_ERR_INVALID_ARG;
+  if (n_q < 1) return KVRING_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(q_pos, 4)) return KVRING_ERR_MISALIGNED;
+  // scratch layout: e4m3 codes [n_q][H][D], then fp32 scales [H][round_up(n_q, 4)]
+  const size_t H = r->rv.H, D = r->rv.D;
+  const size_t q_pad = round_up((size_t)n_q, 4);
+  const size_t scale_off = round_up((size_t)n_q * H * D, 1024);
+  if (scale_off + H * q_pad * sizeof(float) > (size_t)KVRING_NOALLOC_SCRATCH_BYTES) return KVRING_ERR_SCRATCH_LIMIT;
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev != r->device) return KVRING_ERR_INVALID_ARG;
+  uint8_t* scratch = nullptr;
+  const int s = noalloc_scratch(dev, &scratch);
+  if (s != KVRING_OK) return s;
+  RingView rv = r->rv;
+  rv.q_codes = scratch;
+  rv.q_scale = reinterpret_cast<float*>(scratch + scale_off);
+  rv.Q_pad = (int)q_pad;
+  CUtensorMap q_map;
+  if (!encode_query_map(&q_map, scratch, rv.H, rv.D, n_q)) return cuda_fail(cudaErrorInvalidValue);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  e = launch_q_prep(rv, q, q_pos, n_q, st);
+  if (e == cudaSuccess)
+    e = launch_fp8_ring_attn(rv, r->maps, q_map, n_q, out, r->cfg.out_dtype == KVRING_OUT_F32, st);
+  return e == cudaSuccess ? KVRING_OK : cuda_fail(e);
+}
+
 int kvring_destroy(kvring* r) {
   delete r;
   return KVRING_OK;
@@ -298,6 +359,8 @@ const char* kvring_status_string(int s) {
     case KVRING_ERR_CUDA: return "CUDA error";
     case KVRING_ERR_WORKSPACE: return "workspace too small";
     case KVRING_ERR_NO_DEVICE: return "no sm_100-family device is current";
+    case KVRING_ERR_SCRATCH_LIMIT:
+      return "request larger than the static scratch of kvring_attend_noalloc (KVRING_NOALLOC_SCRATCH_BYTES)";
     default: return "unknown status";
   }
 }

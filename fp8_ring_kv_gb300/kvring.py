@@ -20,6 +20,8 @@ KVRING_ERR_UNSUPPORTED = -3
 KVRING_ERR_CUDA = -4
 KVRING_ERR_WORKSPACE = -5
 KVRING_ERR_NO_DEVICE = -6
+KVRING_ERR_SCRATCH_LIMIT = -7
+KVRING_NOALLOC_SCRATCH_BYTES = 8 << 20
 
 KVRING_DEVERR_POS_RANGE = 1
 KVRING_DEVERR_EMPTY = 2
@@ -73,6 +75,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "kvring_write": (ctypes.c_int, [vp, vp, vp, vp, i32, vp]),
         "kvring_reset_positions": (ctypes.c_int, [vp, i32, vp]),
         "kvring_attend": (ctypes.c_int, [vp, vp, vp, i32, vp, vp]),
+        "kvring_attend_noalloc": (ctypes.c_int, [vp, vp, vp, i32, vp, vp]),
         "kvring_destroy": (ctypes.c_int, [vp]),
         "kvring_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         "kvring_last_cuda_error": (ctypes.c_int, []),
@@ -147,6 +150,13 @@ def kvring_reset_positions(handle, d: int, stream=None) -> None:
 def kvring_attend(handle, q, q_pos, n_q: int, out, stream=None) -> None:
     check(load().kvring_attend(handle, _ptr(q), _ptr(q_pos), int(n_q), _ptr(out), _stream(stream)),
           "kvring_attend")
+
+
+def kvring_attend_noalloc(handle, q, q_pos, n_q: int, out, stream=None) -> None:
+    """kvring_attend with the query scratch in the library's fixed device array
+    (no allocation; concurrent calls on one device race on that array)."""
+    check(load().kvring_attend_noalloc(handle, _ptr(q), _ptr(q_pos), int(n_q), _ptr(out), _stream(stream)),
+          "kvring_attend_noalloc")
 
 
 def kvring_destroy(handle) -> None:

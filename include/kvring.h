@@ -167,6 +167,43 @@ int kvring_reset_positions(kvring* r, int32_t d, kvring_stream stream);
 int kvring_attend(kvring* r, const void* q, const int32_t* q_pos, int32_t n_q, void* out,
                   kvring_stream stream);
 
+/*
+ * kvring_attend_noalloc: kvring_attend with its per-call query scratch taken
+ * from a fixed array inside the library instead of from the ring's workspace.
+ * The Runway Characters paper has no counterpart to this call; it is an
+ * addition for callers that cannot allocate device memory when they attend:
+ * a serving loop that reserved all of its device memory at start-up (its
+ * rings were sized with a small max_queries and cannot grow), or a real-time
+ * path that must not call an allocator because cudaMalloc / cudaFree can
+ * block, synchronise the device and take unbounded time.  This call
+ * allocates nothing: no cudaMalloc / cudaFree, no memory pool, no library
+ * that allocates (PyTorch's included), and it leaves the workspace's query
+ * scratch untouched.
+ *
+ *   arguments, output and results: as kvring_attend, except that n_q is not
+ *   bounded by the ring's max_queries but by the static scratch:
+ *     round_up(n_q * H * D, 1024) + H * round_up(n_q, 4) * 4
+ *       <= KVRING_NOALLOC_SCRATCH_BYTES (8 MiB)
+ *   e.g. up to 2,647 queries at 24 heads x 128.  A larger request returns
+ *   KVRING_ERR_SCRATCH_LIMIT before anything is enqueued.
+ *
+ * The scratch is one array per device for the whole process.  Calls that
+ * can overlap in time on one device (two streams, two host threads, two
+ * rings) share it and race: order them on one stream or with events.  Calls
+ * on one stream are safe.  Nothing in the scratch has to start at zero:
+ * each call's first kernel writes every query row and scale that its second
+ * kernel reads, and rows past n_q come from the tensor copy's zero fill.
+ *
+ * Set-up: the first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current, once per device); that
+ * first call should come before any stream capture begins.  The ring's
+ * device must be the current device (else KVRING_ERR_INVALID_ARG).
+ */
+#define KVRING_NOALLOC_SCRATCH_BYTES (8u << 20)
+enum { KVRING_ERR_SCRATCH_LIMIT = -7 /* request larger than kvring_attend_noalloc's static scratch */ };
+int kvring_attend_noalloc(kvring* r, const void* q, const int32_t* q_pos, int32_t n_q, void* out,
+                          kvring_stream stream);
+
 /* Free the host handle (the workspace stays the caller's). NULL is allowed. */
 int kvring_destroy(kvring* r);
 

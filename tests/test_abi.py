@@ -95,7 +95,7 @@ def test_workspace_bytes_rejects_bad_axes(lib):
 
 def test_status_strings(lib):
     codes = [K.KVRING_OK, K.KVRING_ERR_INVALID_ARG, K.KVRING_ERR_MISALIGNED, K.KVRING_ERR_UNSUPPORTED,
-             K.KVRING_ERR_CUDA, K.KVRING_ERR_WORKSPACE, K.KVRING_ERR_NO_DEVICE]
+             K.KVRING_ERR_CUDA, K.KVRING_ERR_WORKSPACE, K.KVRING_ERR_NO_DEVICE, K.KVRING_ERR_SCRATCH_LIMIT]
     texts = [lib.kvring_status_string(c).decode() for c in codes]
     assert len(set(texts)) == len(texts) and all(texts)
     assert lib.kvring_status_string(12345).decode() == "unknown status"
@@ -128,6 +128,7 @@ def test_calls_on_null_handle(lib):
     assert lib.kvring_write(None, p, p, p, 1, None) == K.KVRING_ERR_INVALID_ARG
     assert lib.kvring_reset_positions(None, 5, None) == K.KVRING_ERR_INVALID_ARG
     assert lib.kvring_attend(None, p, p, 1, p, None) == K.KVRING_ERR_INVALID_ARG
+    assert lib.kvring_attend_noalloc(None, p, p, 1, p, None) == K.KVRING_ERR_INVALID_ARG
     assert lib.kvring_destroy(None) == K.KVRING_OK
     out3 = (ctypes.c_int32 * 3)()
     assert lib.kvring_debug_state(None, None, out3) == K.KVRING_ERR_INVALID_ARG

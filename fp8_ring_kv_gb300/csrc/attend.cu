@@ -8,35 +8,37 @@
 // head), from the query preparation kernel (query scratch of the workspace).
 // One block per (tile of 128 queries, head).  The slots are visited in tiles
 // of 128 in storage order: attention is a sum over the valid slots, so the
-// ring's wrap needs no reordering, and slots >= n_valid are masked.  The
-// tiles are split between two streams (the first and the second half of the
-// tiles), each with its own softmax warpgroup, running maximum, running sum
-// and O accumulator; the two partial results are merged at the end.  While
-// one stream computes its softmax the tensor cores work for the other.
+// ring's wrap needs no reordering, and slots >= n_valid are masked.
 //
 //   S_j  = Qcodes . Kcodes_j^T            tcgen05 kind::f8f6f4, fp32 in TMEM
 //   t    = S_j * s_k (per column);  logit*log2(e) = t * s_q * log2(e)/sqrt(D)
 //   online softmax in base 2: e = exp2(t*r - m + c), l += e, with a running
 //   row maximum m that is only raised (and O rescaled) when a tile's maximum
-//   exceeds it by more than 2^8, so e <= 2^8 * 2^c; a thread loads its whole
-//   S row of the tile once and works on registers
-//   P    = e * s_v (per column) rounded to fp16, written over S_j in TMEM
-//   O   += P . Vcodes_j                    tcgen05 kind::f16 (A = P from TMEM)
-//   out  = (O_0 a_0 + O_1 a_1) / (l_0 a_0 + l_1 a_1),  a_i = exp2(m_i - max m)
+//   exceeds it by more than 2^8, so e <= 2^8 * 2^c
+//   P_j  = e * s_v (per column) rounded to fp16, in TMEM
+//   O   += P_j . Vcodes_j                  tcgen05 kind::f16 (A = P from TMEM)
+//   out  = O / l
 // The e4m3 V codes are widened to fp16 in shared memory (exact) because the
 // fp16 MMA takes both operands in fp16; P in fp16 keeps the weighted sum of V
 // within the accuracy that e4m3 weights would lose.  2^c is a per-head power of
 // two (cancelling between O and l) that keeps P within fp16 range.
 //
-// Warp roles (384 threads):
-//   warps 0-3   stream 0 softmax, thread r owns query row r (TMEM lane r)
-//   warps 4-7   stream 1 softmax, same rows; both groups finally run the
-//               merge, each for half of the output columns
-//   warps 8-9   the per-head fp16 range factor, then the per-tile widening
-//               of V to fp16
-//   warp 10     TMA producer (the e4m3 query tile, then K, V codes and their
-//               scales, 4 stages)
-//   warp 11     TMEM allocation and MMA issue
+// Pipeline.  S and P have two TMEM buffers each (S: 2 x 128 columns, P: 2 x
+// 64, O: 128).  The MMA sequence is QK_0, QK_1, PV_0, QK_2, PV_1, QK_3, ...:
+// while the softmax works on tile j the tensor cores run PV_{j-1} and
+// QK_{j+1}, and each MMA waits only for the softmax of the tile it consumes or
+// frees.  TMEM lane quarter q can only be read by the warps of SM
+// sub-partition q, so the softmax of rows 32q .. 32q+31 runs on one
+// sub-partition and its per-tile cost sets the pace.
+//
+// Warp roles (448 threads):
+//   warps 0-7   softmax: warp w serves the 16-lane half w/4 of TMEM lane
+//               quarter w%4; finally the output, half of the columns each
+//   warps 8-11  the per-head fp16 range factor, then the per-tile widening
+//               of V to fp16 (one warp per SM sub-partition)
+//   warp 12     TMA producer (the e4m3 query tile, then K, V codes into 4
+//               stages and their scales into 8)
+//   warp 13     TMEM allocation and MMA issue
 #include <cfloat>
 
 #include "common.cuh"
@@ -47,14 +49,18 @@ namespace kvring_dev {
 constexpr int BM = 128;           // query rows per block
 constexpr int BN = 128;           // slots per tile
 constexpr int NSTAGE = 4;         // fp8 K/V stages
-constexpr int ATT_THREADS = 384;
-constexpr int CONV_THREADS = 64;
-constexpr int WARP_TMA = 10;
-constexpr int WARP_MMA = 11;
-constexpr int SOFT_THREADS = 256;
+constexpr int NSC = 8;            // scale stages (held until the tile's softmax ends)
+constexpr int ATT_THREADS = 448;
+constexpr int SOFT_WARPS = 8;
+constexpr int SOFT_THREADS = 32 * SOFT_WARPS;
+constexpr int CONV_WARPS = 4;
+constexpr int CONV_THREADS = 32 * CONV_WARPS;
+constexpr int WARP_TMA = SOFT_WARPS + CONV_WARPS;
+constexpr int WARP_MMA = WARP_TMA + 1;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t TM_S = 0;      // stream s: fp32 S / fp16 P at columns 128 s
-constexpr uint32_t TM_O = 256;    // stream s: fp32 O at columns 256 + 128 s
+constexpr uint32_t TM_S = 0;      // S buffer b: fp32 [128 lanes][128] at columns 128 b
+constexpr uint32_t TM_P = 256;    // P buffer b: fp16 pairs [128 lanes][64] at columns 256 + 64 b
+constexpr uint32_t TM_O = 384;    // O: fp32 [128 lanes][D]
 constexpr float kLazyRescale = 8.0f;   // log2 of the largest unnormalised weight
 
 template <int D>
@@ -62,13 +68,11 @@ struct AttnLayout {
   static constexpr int Q = 0;                            // e4m3 [BM][D], K-major swizzled
   static constexpr int K0 = Q + BM * D;                  // NSTAGE x e4m3 [BN][D]
   static constexpr int V0 = K0 + NSTAGE * BN * D;        // NSTAGE x e4m3 [BN][D]
-  static constexpr int VH0 = V0 + NSTAGE * BN * D;       // per stream fp16 [BN][D], MN-major swizzled
-  static constexpr int SK0 = VH0 + 2 * BN * D * 2;       // NSTAGE x fp32 [BN]
-  static constexpr int SV0 = SK0 + NSTAGE * BN * 4;
-  static constexpr int SQ = SV0 + NSTAGE * BN * 4;       // fp32 [BM]
-  static constexpr int ML = SQ + BM * 4;                 // fp32 [2 streams][2 (m, l)][BM]
-  static constexpr int BAR = ML + 4 * BM * 4;
-  static constexpr int NBAR = 2 * NSTAGE + 13;
+  static constexpr int VH0 = V0 + NSTAGE * BN * D;       // 2 x fp16 [BN][D], MN-major swizzled
+  static constexpr int SC0 = VH0 + 2 * BN * D * 2;       // NSC x fp32 {s_k [BN], s_v [BN]}
+  static constexpr int ML = SC0 + NSC * 2 * BN * 4;      // fp32 row sums [BM]
+  static constexpr int BAR = ML + BM * 4;
+  static constexpr int NBAR = 2 * NSTAGE + 2 * NSC + 9 + 4;
   static constexpr int MISC = BAR + NBAR * 8;
   static constexpr int BYTES = MISC + 64;
   static constexpr int ALLOC = BYTES + 1024;             // slack for 1024-byte alignment
@@ -92,28 +96,6 @@ __device__ __forceinline__ uint64_t kmajor_desc(uint32_t addr) {
     return make_sdesc_sw64(addr, 16, 512);
 }
 
-// The tiles in the order the producer, the widening warps and the MMA issuer
-// walk them: (stream 0, tile 0), (stream 1, tile 0), (stream 0, tile 1), ...
-// Stream 0 owns tiles [0, T0), stream 1 tiles [T0, T), T0 = ceil(T/2); only
-// stream 0 can be one tile longer.
-struct TileSeq {
-  int T0, T1;
-  __device__ explicit TileSeq(int T) : T0((T + 1) >> 1), T1(T - ((T + 1) >> 1)) {}
-  __device__ int count() const { return T0 + T1; }
-  // position in the walk of (stream s, tile j of that stream)
-  __device__ int pos(int s, int j) const { return j < T1 ? 2 * j + s : 2 * T1 + (j - T1); }
-  __device__ void at(int u, int& s, int& j) const {
-    if (u < 2 * T1) {
-      s = u & 1;
-      j = u >> 1;
-    } else {
-      s = 0;
-      j = T1 + (u - 2 * T1);
-    }
-  }
-  __device__ int tile(int s, int j) const { return s * T0 + j; }
-};
-
 template <int D>
 __global__ void __launch_bounds__(ATT_THREADS, 1)
     fp8_ring_attn_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -126,19 +108,21 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
   // so the compiler keeps every access below in the shared address space
   uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + LY::BAR);
-  uint64_t* kv_full = bars + 0;                 // [NSTAGE]
-  uint64_t* kv_empty = bars + NSTAGE;           // [NSTAGE]
-  uint64_t* s_full = bars + 2 * NSTAGE;         // [2 streams]
-  uint64_t* vh_full = s_full + 2;               // [2 streams]
-  uint64_t* p_full = s_full + 4;                // [2 streams]
-  uint64_t* pv_done = s_full + 6;               // [2 streams]
-  uint64_t* q_full = s_full + 8;
-  uint64_t* ml_xchg = s_full + 9;               // [4 warp pairs]
+  uint64_t* kv_full = bars;                     // [NSTAGE] K, V codes landed
+  uint64_t* kv_empty = kv_full + NSTAGE;        // [NSTAGE] K read by QK, V widened
+  uint64_t* sc_full = kv_empty + NSTAGE;        // [NSC] scales landed
+  uint64_t* sc_empty = sc_full + NSC;           // [NSC] the tile's softmax is done
+  uint64_t* s_full = sc_empty + NSC;            // [2] QK done into S buffer b
+  uint64_t* p_full = s_full + 2;                // [2] P in buffer b, S buffer b read
+  uint64_t* pv_done = p_full + 2;               // [2] PV from P buffer b done
+  uint64_t* vh_full = pv_done + 2;              // [2] fp16 V buffer b written
+  uint64_t* q_full = vh_full + 2;               // query tile + range factor
+  uint64_t* ml_xchg = q_full + 1;               // [4] per lane quarter
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + LY::MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + LY::MISC + 4);
   int* maxsv_bits = reinterpret_cast<int*>(sm + LY::MISC + 8);
   float* cv_smem = reinterpret_cast<float*>(sm + LY::MISC + 12);   // log2 of the per-head weight factor
-  float* ml = reinterpret_cast<float*>(sm + LY::ML);
+  float* lrow = reinterpret_cast<float*>(sm + LY::ML);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -148,20 +132,23 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
   const int H = rv.H;
   const int n_valid = rv.state[ST_NVALID];
   const int T = (n_valid + BN - 1) / BN;
-  const TileSeq seq(T);
 
   if (tid == 0) {
     for (int i = 0; i < NSTAGE; ++i) {
       mbar_init(&kv_full[i], 1);
-      mbar_init(&kv_empty[i], 1 + 2 + 4);   // QK commit, 2 widening warps, 4 softmax warps
+      mbar_init(&kv_empty[i], 1 + CONV_WARPS);   // QK commit, the widening warps
+    }
+    for (int i = 0; i < NSC; ++i) {
+      mbar_init(&sc_full[i], 1);
+      mbar_init(&sc_empty[i], SOFT_WARPS);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&vh_full[i], 2);
-      mbar_init(&p_full[i], 4);
+      mbar_init(&p_full[i], SOFT_WARPS);
       mbar_init(&pv_done[i], 1);
+      mbar_init(&vh_full[i], CONV_WARPS);
     }
-    mbar_init(q_full, 1 + 2);   // the query tile's TMA, 2 widening warps (range factor)
+    mbar_init(q_full, 1 + CONV_WARPS);   // the query tile's TMA, the widening warps (range factor)
     for (int i = 0; i < 4; ++i) mbar_init(&ml_xchg[i], 2);
     *abort_flag = 0;
     *maxsv_bits = 0;
@@ -193,187 +180,235 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       }
     }
     if (tid == 0 && qt == 0 && h == 0) atomicOr(&rv.state[ST_ERR], DEVERR_EMPTY);
-  } else if (warp < 8) {
-    // ======================================================== softmax of stream g
-    const int g = warp >> 2;
-    const int r = tid & 127;                     // query row = TMEM lane
-    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-    const uint32_t s_addr = tmem + lane_off + TM_S + g * 128;
-    const uint32_t o_addr = tmem + lane_off + TM_O + g * 128;
+  } else if (warp < SOFT_WARPS) {
+    // ======================================================== softmax
+    // Warp (hf, quarter) reads its 16 TMEM lanes in the 16x256b shape: thread
+    // t holds rows t/4 (a) and t/4 + 8 (b) of the half and, of each group of
+    // 8 columns, columns 2(t%4) and 2(t%4) + 1.  Four threads share a row and
+    // each needs only its 32 columns' scales.
+    const int hf = warp >> 2;
+    const int quarter = warp & 3;
+    const int c4 = lane & 3;
+    const int r4 = lane >> 2;
+    const uint32_t lanes = (uint32_t)(32 * quarter + 16 * hf) << 16;
+    const uint32_t o_addr = tmem + lanes + TM_O;
     constexpr float kRowC = (D == 128 ? 0.08838834764831845f : 0.125f) * 1.4426950408889634f;
-    const int qrow = qt * BM + r;
-    const float sq = qrow < n_q ? rv.q_scale[(size_t)h * rv.Q_pad + qrow] : 0.0f;
+    float rq[2], m_run[2];
+    float2 lsum[2];
+#pragma unroll
+    for (int sb = 0; sb < 2; ++sb) {
+      const int qrow = qt * BM + 32 * quarter + 16 * hf + r4 + 8 * sb;
+      const float sq = qrow < n_q ? rv.q_scale[(size_t)h * rv.Q_pad + qrow] : 0.0f;
+      rq[sb] = sq > 0.0f ? sq * kRowC : 1.0f;
+      m_run[sb] = -INFINITY;
+      lsum[sb] = make_float2(0.0f, 0.0f);
+    }
     bool ok = mbar_wait(q_full, 0, abort_flag);
-    const float rq = sq > 0.0f ? sq * kRowC : 1.0f;
     const float log2cv = *cv_smem;
-    const float2 rq2 = make_float2(rq, rq);
-    const int Tg = g == 0 ? seq.T0 : seq.T1;
-    float m_run = -INFINITY;
-    float2 lacc = make_float2(0.0f, 0.0f);
-    for (int j = 0; ok && j < Tg; ++j) {
-      const int u = seq.pos(g, j);
-      const int st = u % NSTAGE;
-      if (!mbar_wait(&kv_full[st], (u / NSTAGE) & 1, abort_flag) || !mbar_wait(&s_full[g], j & 1, abort_flag)) {
+    for (int j = 0; ok && j < T; ++j) {
+      const int b = j & 1;
+      const int sc = j % NSC;
+      if (!mbar_wait(&sc_full[sc], (j / NSC) & 1, abort_flag) || !mbar_wait(&s_full[b], (j >> 1) & 1, abort_flag)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const float4* sk4 = reinterpret_cast<const float4*>(sm + LY::SK0 + st * BN * 4);
-      const float4* sv4 = reinterpret_cast<const float4*>(sm + LY::SV0 + st * BN * 4);
-      const int valid = min(BN, n_valid - seq.tile(g, j) * BN);
-      // The whole row of the tile (128 columns) comes in with one wait, so the
-      // maximum and the weights run on registers with 32-way parallelism.
-      // If the tile maximum exceeds the running maximum by more than 2^8
-      // (always on the first tile), the maximum is raised and O rescaled.
-      // P (fp16 pairs, 64 columns) is then written over the S buffer.
-      float x[128];
-      tmem_ld32(s_addr + 0, *reinterpret_cast<uint32_t(*)[32]>(x + 0));
-      tmem_ld32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(x + 32));
-      tmem_ld32(s_addr + 64, *reinterpret_cast<uint32_t(*)[32]>(x + 64));
-      tmem_ld32(s_addr + 96, *reinterpret_cast<uint32_t(*)[32]>(x + 96));
-      tmem_wait_ld();
+      const uint32_t s_addr = tmem + lanes + TM_S + 128 * b;
+      // column 8k + 2*c4 of the tile's scales at [8k]
+      const float* skp = reinterpret_cast<const float*>(sm + LY::SC0 + sc * 2 * BN * 4) + 2 * c4;
+      const float* svp = skp + BN;
+      const int valid = min(BN, n_valid - j * BN);
+      // The weights use the running maximum from the earlier tiles while the
+      // tile's own maximum is found alongside; each thread compares the
+      // maximum of its own columns, which exceeds the bound whenever the
+      // row's does.  Only then (and always on the first tile) is the row
+      // maximum formed, raised, O and the sums rescaled, and the tile
+      // recomputed from S, which stays in TMEM until this tile's end.
+      uint32_t pk[32];
+      float2 la = make_float2(0.0f, 0.0f), lb = la;
+      for (int pass = (j == 0 ? 1 : 0); pass < 2; ++pass) {
+        uint32_t xr[64];
+        tmem_ld_16x256b_x16(s_addr, xr);
+        float* x = reinterpret_cast<float*>(xr);
+        {
+          float2 sk[16];
 #pragma unroll
-      for (int i = 0; i < 128; i += 4) {
-        const float4 k4 = sk4[i >> 2];
-        const float2 t0 = mul2(make_float2(x[i], x[i + 1]), make_float2(k4.x, k4.y));
-        const float2 t1 = mul2(make_float2(x[i + 2], x[i + 3]), make_float2(k4.z, k4.w));
-        x[i] = t0.x;
-        x[i + 1] = t0.y;
-        x[i + 2] = t1.x;
-        x[i + 3] = t1.y;
-      }
-      if (valid < BN) {
+          for (int k = 0; k < 16; ++k) sk[k] = *reinterpret_cast<const float2*>(skp + 8 * k);
 #pragma unroll
-        for (int i = 0; i < 128; ++i)
-          if (i >= valid) x[i] = -INFINITY;
-      }
-      float mt;
-      {
-        float m[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) m[i] = max3f(x[i], x[i + 16], fmaxf(x[i + 32], x[i + 48]));
-#pragma unroll
-        for (int i = 0; i < 16; ++i) m[i] = max3f(m[i], fmaxf(x[i + 64], x[i + 80]), fmaxf(x[i + 96], x[i + 112]));
-#pragma unroll
-        for (int w = 8; w > 0; w >>= 1)
-#pragma unroll
-          for (int i = 0; i < w; ++i) m[i] = fmaxf(m[i], m[i + w]);
-        mt = m[0];
-      }
-      const float m_tile = mt * rq;
-      const bool grow = (j == 0) || (m_tile > m_run + kLazyRescale);
-      if (__any_sync(0xFFFFFFFFu, grow)) {
-        const float m_new = fmaxf(m_run, m_tile);
-        if (j > 0) {
-          // O holds rows weighted by exp2(-m_run): bring them to exp2(-m_new)
-          if (!mbar_wait(&pv_done[g], (j - 1) & 1, abort_flag)) {
-            ok = false;
-            break;
+          for (int k = 0; k < 16; ++k) {
+            const float2 ta = mul2(make_float2(x[4 * k], x[4 * k + 1]), sk[k]);
+            const float2 tb = mul2(make_float2(x[4 * k + 2], x[4 * k + 3]), sk[k]);
+            x[4 * k] = ta.x;
+            x[4 * k + 1] = ta.y;
+            x[4 * k + 2] = tb.x;
+            x[4 * k + 3] = tb.y;
           }
-          tc_fence_after();
-          const float alpha = ex2f(m_run - m_new);
-#pragma unroll 1
-          for (int c0 = 0; c0 < D; c0 += 16) {
-            uint32_t o[16];
-            tmem_ld16(o_addr + c0, o);
-            tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-            tmem_st16(o_addr + c0, o);
-          }
-          tmem_wait_st();
-          lacc.x *= alpha;
-          lacc.y *= alpha;
         }
-        m_run = m_new;
-      }
-      const float2 moff = make_float2(log2cv - m_run, log2cv - m_run);
-      uint32_t pk[64];
-      float2 l2 = make_float2(0.0f, 0.0f);
+        if (valid < BN) {
 #pragma unroll
-      for (int i = 0; i < 128; i += 4) {
-        const float4 v4 = sv4[i >> 2];
-        const float2 a0 = fma2(make_float2(x[i], x[i + 1]), rq2, moff);
-        const float2 a1 = fma2(make_float2(x[i + 2], x[i + 3]), rq2, moff);
-        const float2 e0 = make_float2(ex2f(a0.x), ex2f(a0.y));
-        const float2 e1 = make_float2(ex2f(a1.x), ex2f(a1.y));
-        lacc = add2(lacc, e0);
-        l2 = add2(l2, e1);
-        const float2 p0 = mul2(e0, make_float2(v4.x, v4.y));
-        const float2 p1 = mul2(e1, make_float2(v4.z, v4.w));
-        pk[i >> 1] = cvt_f16x2(p0.x, p0.y);
-        pk[(i >> 1) + 1] = cvt_f16x2(p1.x, p1.y);
-      }
-      lacc = add2(lacc, l2);
+          for (int k = 0; k < 16; ++k)
 #pragma unroll
-      for (int cb = 0; cb < 4; ++cb) tmem_st16(s_addr + cb * 16, *reinterpret_cast<uint32_t(*)[16]>(pk + 16 * cb));
-      tmem_wait_st();
+            for (int i = 0; i < 4; ++i)
+              if (8 * k + 2 * c4 + (i & 1) >= valid) x[4 * k + i] = -INFINITY;
+        }
+        // maxima of rows a and b over this thread's columns (times the row factor)
+        float ma, mb;
+        {
+          float pa[8], pb[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            pa[i] = max3f(x[8 * i], x[8 * i + 1], fmaxf(x[8 * i + 4], x[8 * i + 5]));
+            pb[i] = max3f(x[8 * i + 2], x[8 * i + 3], fmaxf(x[8 * i + 6], x[8 * i + 7]));
+          }
+          ma = max3f(max3f(pa[0], pa[1], pa[2]), max3f(pa[3], pa[4], pa[5]), fmaxf(pa[6], pa[7])) * rq[0];
+          mb = max3f(max3f(pb[0], pb[1], pb[2]), max3f(pb[3], pb[4], pb[5]), fmaxf(pb[6], pb[7])) * rq[1];
+        }
+        if (pass == 1) {
+          // row maxima over the four threads of each row
+          ma = fmaxf(ma, __shfl_xor_sync(0xFFFFFFFFu, ma, 1));
+          mb = fmaxf(mb, __shfl_xor_sync(0xFFFFFFFFu, mb, 1));
+          ma = fmaxf(ma, __shfl_xor_sync(0xFFFFFFFFu, ma, 2));
+          mb = fmaxf(mb, __shfl_xor_sync(0xFFFFFFFFu, mb, 2));
+          const bool grow0 = j == 0 || ma > m_run[0] + kLazyRescale;
+          const bool grow1 = j == 0 || mb > m_run[1] + kLazyRescale;
+          const float mn0 = grow0 ? fmaxf(m_run[0], ma) : m_run[0];
+          const float mn1 = grow1 ? fmaxf(m_run[1], mb) : m_run[1];
+          if (j > 0) {
+            // O holds rows weighted by exp2(-m_run): once PV_{j-1} (and so
+            // every earlier PV) is done, bring them to exp2(-m_new)
+            if (!mbar_wait(&pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const float al0 = ex2f(m_run[0] - mn0);
+            const float al1 = ex2f(m_run[1] - mn1);
+#pragma unroll 1
+            for (int c0 = 0; c0 < D; c0 += 32) {
+              uint32_t o[16];
+              tmem_ld_16x256b_x4(o_addr + c0, o);
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                o[4 * k] = __float_as_uint(__uint_as_float(o[4 * k]) * al0);
+                o[4 * k + 1] = __float_as_uint(__uint_as_float(o[4 * k + 1]) * al0);
+                o[4 * k + 2] = __float_as_uint(__uint_as_float(o[4 * k + 2]) * al1);
+                o[4 * k + 3] = __float_as_uint(__uint_as_float(o[4 * k + 3]) * al1);
+              }
+              tmem_st_16x256b_x4(o_addr + c0, o);
+            }
+            lsum[0] = mul2(lsum[0], make_float2(al0, al0));
+            lsum[1] = mul2(lsum[1], make_float2(al1, al1));
+          }
+          m_run[0] = mn0;
+          m_run[1] = mn1;
+        } else if (__any_sync(0xFFFFFFFFu, ma > m_run[0] + kLazyRescale || mb > m_run[1] + kLazyRescale)) {
+          continue;   // -> pass 1
+        }
+        // weights e = exp2(t * rq + c - m), P = e * s_v in fp16 pairs; the
+        // pair of row a at repetition k goes to P column 4k + t%4 of row a
+        const float2 rqa = make_float2(rq[0], rq[0]);
+        const float2 rqb = make_float2(rq[1], rq[1]);
+        const float2 moa = make_float2(log2cv - m_run[0], log2cv - m_run[0]);
+        const float2 mob = make_float2(log2cv - m_run[1], log2cv - m_run[1]);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const float2 aa = fma2(make_float2(x[4 * k], x[4 * k + 1]), rqa, moa);
+          const float2 ab = fma2(make_float2(x[4 * k + 2], x[4 * k + 3]), rqb, mob);
+          x[4 * k] = aa.x;
+          x[4 * k + 1] = aa.y;
+          x[4 * k + 2] = ab.x;
+          x[4 * k + 3] = ab.y;
+        }
+#pragma unroll
+        for (int i = 0; i < 64; ++i) x[i] = ex2f(x[i]);
+        float2 la0 = make_float2(0.0f, 0.0f), la1 = la0, lb0 = la0, lb1 = la0;
+#pragma unroll
+        for (int k = 0; k < 16; k += 2) {
+          la0 = add2(la0, make_float2(x[4 * k], x[4 * k + 1]));
+          lb0 = add2(lb0, make_float2(x[4 * k + 2], x[4 * k + 3]));
+          la1 = add2(la1, make_float2(x[4 * k + 4], x[4 * k + 5]));
+          lb1 = add2(lb1, make_float2(x[4 * k + 6], x[4 * k + 7]));
+        }
+        la = add2(la0, la1);
+        lb = add2(lb0, lb1);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const float2 sv = *reinterpret_cast<const float2*>(svp + 8 * k);
+          const float2 pa2 = mul2(make_float2(x[4 * k], x[4 * k + 1]), sv);
+          const float2 pb2 = mul2(make_float2(x[4 * k + 2], x[4 * k + 3]), sv);
+          pk[2 * k] = cvt_f16x2(pa2.x, pa2.y);
+          pk[2 * k + 1] = cvt_f16x2(pb2.x, pb2.y);
+        }
+        break;
+      }
+      if (!ok) break;
+      lsum[0] = add2(lsum[0], la);
+      lsum[1] = add2(lsum[1], lb);
+      // P buffer b is free once PV_{j-2} is done
+      if (j >= 2 && !mbar_wait(&pv_done[b], ((j - 2) >> 1) & 1, abort_flag)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      tmem_st_16x128b_x16(tmem + lanes + TM_P + 64 * b, pk);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(&p_full[g]);
-        mbar_arrive(&kv_empty[st]);
+        mbar_arrive(&p_full[b]);
+        mbar_arrive(&sc_empty[sc]);
       }
     }
-    // ======================================================== merge + epilogue
-    // Warps w and w+4 hold the same rows: they swap (m, l), then each writes
-    // half of the output columns from both streams' O.
-    float* mine = ml + g * 2 * BM;
-    float* other = ml + (g ^ 1) * 2 * BM;
-    const float l_mine = lacc.x + lacc.y;
-    mine[r] = m_run;
-    mine[BM + r] = l_mine;
+    // ======================================================== output
+    // Each row's sum is spread over the four threads that share it.  The two
+    // warps of a lane quarter publish the sums of their rows in shared
+    // memory; each then writes half of the output columns of the quarter's
+    // 32 rows, one row per thread (thread t <-> lane 32*quarter + t).
+#pragma unroll
+    for (int sb = 0; sb < 2; ++sb) {
+      float l = lsum[sb].x + lsum[sb].y;
+      l += __shfl_xor_sync(0xFFFFFFFFu, l, 1);
+      l += __shfl_xor_sync(0xFFFFFFFFu, l, 2);
+      if (c4 == 0) lrow[32 * quarter + 16 * hf + r4 + 8 * sb] = l;
+    }
     __syncwarp();
-    if (lane == 0) mbar_arrive(&ml_xchg[warp & 3]);
-    ok = ok && mbar_wait(&ml_xchg[warp & 3], 0, abort_flag);
-    const float m_o = other[r];
-    const float l_o = other[BM + r];
-    const float m0 = g == 0 ? m_run : m_o;
-    const float m1 = g == 0 ? m_o : m_run;
-    const float l0 = g == 0 ? l_mine : l_o;
-    const float l1 = g == 0 ? l_o : l_mine;
-    const bool has1 = seq.T1 > 0;
-    ok = ok && mbar_wait(&pv_done[0], (seq.T0 - 1) & 1, abort_flag);
-    ok = ok && (!has1 || mbar_wait(&pv_done[1], (seq.T1 - 1) & 1, abort_flag));
+    if (lane == 0) mbar_arrive(&ml_xchg[quarter]);
+    ok = ok && mbar_wait(&ml_xchg[quarter], 0, abort_flag);
+    const int r = 32 * quarter + lane;
+    const float l_row = lrow[r];
+    ok = ok && mbar_wait(&pv_done[(T - 1) & 1], ((T - 1) >> 1) & 1, abort_flag);
     if (ok) {
       tc_fence_after();
-      const float M = has1 ? fmaxf(m0, m1) : m0;
-      const float a0 = ex2f(m0 - M);
-      const float a1 = has1 ? ex2f(m1 - M) : 0.0f;
-      const float inv_l = 1.0f / (l0 * a0 + l1 * a1);
-      const float w0 = a0 * inv_l;
-      const float w1 = a1 * inv_l;
+      const float inv_l = 1.0f / l_row;
       const int qi = qt * BM + r;
-      const uint32_t o0_addr = tmem + lane_off + TM_O;
-      const uint32_t o1_addr = tmem + lane_off + TM_O + 128;
+      const uint32_t row_o = tmem + ((uint32_t)(32 * quarter) << 16) + TM_O;
       uint8_t* orow = static_cast<uint8_t*>(out) + ((size_t)qi * H + h) * (size_t)D * (out_f32 ? 4 : 2);
 #pragma unroll 1
-      for (int c0 = g * (D / 2); c0 < (g + 1) * (D / 2); c0 += 16) {
+      for (int c0 = hf * (D / 2); c0 < (hf + 1) * (D / 2); c0 += 32) {
         uint32_t o0[16], o1[16];
-        tmem_ld16(o0_addr + c0, o0);
-        tmem_ld16(o1_addr + c0, o1);
-        tmem_wait_ld();
-        float v[16];
+        tmem_ld2_32x32b_x16(row_o + c0, row_o + c0 + 16, o0, o1);
+        float v[32];
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          v[i] = has1 ? __uint_as_float(o0[i]) * w0 + __uint_as_float(o1[i]) * w1 : __uint_as_float(o0[i]) * w0;
+        for (int i = 0; i < 16; ++i) {
+          v[i] = __uint_as_float(o0[i]) * inv_l;
+          v[16 + i] = __uint_as_float(o1[i]) * inv_l;
+        }
         if (qi < n_q) {
           if (out_f32) {
             uint4* dst = reinterpret_cast<uint4*>(orow + c0 * 4);
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
+            for (int i = 0; i < 8; ++i)
               dst[i] = make_uint4(__float_as_uint(v[4 * i]), __float_as_uint(v[4 * i + 1]),
                                   __float_as_uint(v[4 * i + 2]), __float_as_uint(v[4 * i + 3]));
           } else {
-            uint32_t pb[8];
+            uint32_t pb[16];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
+            for (int i = 0; i < 16; ++i) {
               const __nv_bfloat162 v2 = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
               pb[i] = *reinterpret_cast<const uint32_t*>(&v2);
             }
             uint4* dst = reinterpret_cast<uint4*>(orow + c0 * 2);
-            dst[0] = make_uint4(pb[0], pb[1], pb[2], pb[3]);
-            dst[1] = make_uint4(pb[4], pb[5], pb[6], pb[7]);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pb[4 * i], pb[4 * i + 1], pb[4 * i + 2], pb[4 * i + 3]);
           }
         }
       }
@@ -398,7 +433,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
       if (lane == 0) atomicMax(maxsv_bits, __float_as_int(mx));
-      asm volatile("bar.sync 1, 64;" ::: "memory");
+      asm volatile("bar.sync 1, %0;" ::"n"(CONV_THREADS) : "memory");
       if (ct == 0) {
         const float m = __int_as_float(*maxsv_bits);
         // weights reach 2^8 * 2^c; with c = 6 - floor(log2 max s_v) every
@@ -407,21 +442,20 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         c = c < -64 ? -64 : (c > 64 ? 64 : c);
         *cv_smem = (float)c;
       }
-      asm volatile("bar.sync 1, 64;" ::: "memory");
+      asm volatile("bar.sync 1, %0;" ::"n"(CONV_THREADS) : "memory");
       __syncwarp();
       if (lane == 0) mbar_arrive(q_full);
     }
 
     constexpr int CH = D / 16;  // 16-byte e4m3 chunks per slot row
-    for (int u = 0; u < seq.count(); ++u) {
-      int sg, j;
-      seq.at(u, sg, j);
+    for (int u = 0; u < T; ++u) {
       const int st = u % NSTAGE;
+      const int b = u & 1;
       if (!mbar_wait(&kv_full[st], (u / NSTAGE) & 1, abort_flag)) break;
-      // the stream's fp16 V buffer is free once its previous PV has finished
-      if (j >= 1 && !mbar_wait(&pv_done[sg], (j - 1) & 1, abort_flag)) break;
+      // fp16 V buffer b is free once PV_{u-2} is done
+      if (u >= 2 && !mbar_wait(&pv_done[b], ((u - 2) >> 1) & 1, abort_flag)) break;
       const uint8_t* vsrc = sm + LY::V0 + st * BN * D;
-      uint8_t* vdst = sm + LY::VH0 + sg * BN * D * 2;
+      uint8_t* vdst = sm + LY::VH0 + b * BN * D * 2;
       // eight consecutive threads take the same chunk of eight consecutive
       // slots, so their 16-byte reads and writes fall in distinct bank groups
 #pragma unroll
@@ -450,7 +484,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(&vh_full[sg]);
+        mbar_arrive(&vh_full[b]);
         mbar_arrive(&kv_empty[st]);
       }
     }
@@ -459,64 +493,55 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
     if (lane == 0) {
       mbar_arrive_expect_tx(q_full, BM * D);
       tma_load_3d(sm + LY::Q, &tmQ, q_full, 0, h, qt * BM);
-      for (int u = 0; u < seq.count(); ++u) {
-        int sg, j;
-        seq.at(u, sg, j);
+      for (int u = 0; u < T; ++u) {
         const int st = u % NSTAGE;
+        const int sc = u % NSC;
         if (u >= NSTAGE && !mbar_wait(&kv_empty[st], ((u / NSTAGE) - 1) & 1, abort_flag)) break;
-        const int t = seq.tile(sg, j);
-        mbar_arrive_expect_tx(&kv_full[st], 2 * BN * D + 2 * BN * 4);
-        tma_load_3d(sm + LY::K0 + st * BN * D, &tmK, &kv_full[st], 0, t * BN, h);
-        tma_load_3d(sm + LY::V0 + st * BN * D, &tmV, &kv_full[st], 0, t * BN, h);
-        tma_load_2d(sm + LY::SK0 + st * BN * 4, &tmSK, &kv_full[st], t * BN, h);
-        tma_load_2d(sm + LY::SV0 + st * BN * 4, &tmSV, &kv_full[st], t * BN, h);
+        mbar_arrive_expect_tx(&kv_full[st], 2 * BN * D);
+        tma_load_3d(sm + LY::K0 + st * BN * D, &tmK, &kv_full[st], 0, u * BN, h);
+        tma_load_3d(sm + LY::V0 + st * BN * D, &tmV, &kv_full[st], 0, u * BN, h);
+        if (u >= NSC && !mbar_wait(&sc_empty[sc], ((u / NSC) - 1) & 1, abort_flag)) break;
+        mbar_arrive_expect_tx(&sc_full[sc], 2 * BN * 4);
+        tma_load_2d(sm + LY::SC0 + sc * 2 * BN * 4, &tmSK, &sc_full[sc], u * BN, h);
+        tma_load_2d(sm + LY::SC0 + sc * 2 * BN * 4 + BN * 4, &tmSV, &sc_full[sc], u * BN, h);
       }
     }
   } else {
     // ======================================================== MMA issue
-    // Order: QK of both streams' first tiles, then per tile index j:
-    // PV_0(j), QK_0(j+1), PV_1(j), QK_1(j+1).  QK_s(j+1) overwrites the
-    // buffer PV_s(j) reads P from, so it waits for PV_s(j) to finish.
+    // QK_0, QK_1, then per tile j: PV_j once P_j is written, and QK_{j+2}
+    // into the S buffer that the softmax of tile j has finished reading.
     if (lane == 0) {
       constexpr uint32_t idesc_qk = make_idesc(0, 0, 0, 0, BM, BN);   // e4m3 x e4m3, both K-major
       constexpr uint32_t idesc_pv = make_idesc(0, 0, 0, 1, BM, D);    // f16 x f16, V MN-major
       bool ok = mbar_wait(q_full, 0, abort_flag);
       const uint32_t q_addr = smem_u32(sm + LY::Q);
-      auto issue_qk = [&](int sg, int j) -> bool {
-        const int u = seq.pos(sg, j);
+      auto issue_qk = [&](int u) -> bool {
         const int st = u % NSTAGE;
         if (!mbar_wait(&kv_full[st], (u / NSTAGE) & 1, abort_flag)) return false;
-        if (j >= 1 && !mbar_wait(&pv_done[sg], (j - 1) & 1, abort_flag)) return false;
         tc_fence_after();
         const uint32_t ka = smem_u32(sm + LY::K0 + st * BN * D);
 #pragma unroll
         for (int kk = 0; kk < D / 32; ++kk)
-          mma_f8_ss(tmem + TM_S + sg * 128, kmajor_desc<D>(q_addr + kk * 32), kmajor_desc<D>(ka + kk * 32), idesc_qk,
-                    kk > 0 ? 1u : 0u);
-        mma_commit(&s_full[sg]);
+          mma_f8_ss(tmem + TM_S + 128 * (u & 1), kmajor_desc<D>(q_addr + kk * 32), kmajor_desc<D>(ka + kk * 32),
+                    idesc_qk, kk > 0 ? 1u : 0u);
+        mma_commit(&s_full[u & 1]);
         mma_commit(&kv_empty[st]);
         return true;
       };
-      auto issue_pv = [&](int sg, int j) -> bool {
-        if (!mbar_wait(&p_full[sg], j & 1, abort_flag) || !mbar_wait(&vh_full[sg], j & 1, abort_flag)) return false;
+      ok = ok && issue_qk(0);
+      if (T > 1) ok = ok && issue_qk(1);
+      for (int j = 0; ok && j < T; ++j) {
+        const int b = j & 1;
+        if (!mbar_wait(&p_full[b], (j >> 1) & 1, abort_flag) || !mbar_wait(&vh_full[b], (j >> 1) & 1, abort_flag))
+          break;
         tc_fence_after();
-        const uint32_t va = smem_u32(sm + LY::VH0 + sg * BN * D * 2);
+        const uint32_t va = smem_u32(sm + LY::VH0 + b * BN * D * 2);
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
-          mma_f16_ts(tmem + TM_O + sg * 128, tmem + TM_S + sg * 128 + kk * 8,
-                     make_sdesc_sw128(va + kk * 16 * 128, BN * 128, 1024), idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&pv_done[sg]);
-        return true;
-      };
-      ok = ok && issue_qk(0, 0);
-      if (seq.T1 > 0) ok = ok && issue_qk(1, 0);
-      for (int j = 0; ok && j < seq.T0; ++j) {
-        ok = ok && issue_pv(0, j);
-        if (j + 1 < seq.T0) ok = ok && issue_qk(0, j + 1);
-        if (j < seq.T1) {
-          ok = ok && issue_pv(1, j);
-          if (j + 1 < seq.T1) ok = ok && issue_qk(1, j + 1);
-        }
+          mma_f16_ts(tmem + TM_O, tmem + TM_P + 64 * b + kk * 8, make_sdesc_sw128(va + kk * 16 * 128, BN * 128, 1024),
+                     idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&pv_done[b]);
+        if (j + 2 < T) ok = issue_qk(j + 2);
       }
     }
   }

@@ -24,9 +24,9 @@
 // two (cancelling between O and l) that keeps P within fp16 range.
 //
 // Pipeline.  S and P have two TMEM buffers each (S: 2 x 128 columns, P: 2 x
-// 64, O: 128).  The MMA sequence is QK_0, QK_1, PV_0, QK_2, PV_1, QK_3, ...:
-// while the softmax works on tile j the tensor cores run PV_{j-1} and
-// QK_{j+1}, and each MMA waits only for the softmax of the tile it consumes or
+// 64, O: 128).  The MMA sequence is QK_0, QK_1, QK_2, PV_0, QK_3, PV_1, ...:
+// while the softmax works on tile j the tensor cores run QK_{j+1} and
+// PV_{j-1}, and each MMA waits only for the softmax of the tile it consumes or
 // frees.  TMEM lane quarter q can only be read by the warps of SM
 // sub-partition q, so the softmax of rows 32q .. 32q+31 runs on one
 // sub-partition and its per-tile cost sets the pace.
@@ -301,8 +301,6 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
           }
           m_run[0] = mn0;
           m_run[1] = mn1;
-        } else if (__any_sync(0xFFFFFFFFu, ma > m_run[0] + kLazyRescale || mb > m_run[1] + kLazyRescale)) {
-          continue;   // -> pass 1
         }
         // weights e = exp2(t * rq + c - m), P = e * s_v in fp16 pairs; the
         // pair of row a at repetition k goes to P column 4k + t%4 of row a
@@ -339,6 +337,9 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
           pk[2 * k] = cvt_f16x2(pa2.x, pa2.y);
           pk[2 * k + 1] = cvt_f16x2(pb2.x, pb2.y);
         }
+        // decided only now, so that the maxima overlap the exponentials
+        if (pass == 0 && __any_sync(0xFFFFFFFFu, ma > m_run[0] + kLazyRescale || mb > m_run[1] + kLazyRescale))
+          continue;   // -> pass 1
         break;
       }
       if (!ok) break;
@@ -508,8 +509,8 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
     }
   } else {
     // ======================================================== MMA issue
-    // QK_0, QK_1, then per tile j: PV_j once P_j is written, and QK_{j+2}
-    // into the S buffer that the softmax of tile j has finished reading.
+    // QK_0, QK_1, then per tile j, once the softmax of tile j is done: QK_{j+2}
+    // into the S buffer it has finished reading, then PV_j.
     if (lane == 0) {
       constexpr uint32_t idesc_qk = make_idesc(0, 0, 0, 0, BM, BN);   // e4m3 x e4m3, both K-major
       constexpr uint32_t idesc_pv = make_idesc(0, 0, 0, 1, BM, D);    // f16 x f16, V MN-major
@@ -535,13 +536,13 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         if (!mbar_wait(&p_full[b], (j >> 1) & 1, abort_flag) || !mbar_wait(&vh_full[b], (j >> 1) & 1, abort_flag))
           break;
         tc_fence_after();
+        if (j + 2 < T && !issue_qk(j + 2)) break;
         const uint32_t va = smem_u32(sm + LY::VH0 + b * BN * D * 2);
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
           mma_f16_ts(tmem + TM_O, tmem + TM_P + 64 * b + kk * 8, make_sdesc_sw128(va + kk * 16 * 128, BN * 128, 1024),
                      idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&pv_done[b]);
-        if (j + 2 < T) ok = issue_qk(j + 2);
       }
     }
   }

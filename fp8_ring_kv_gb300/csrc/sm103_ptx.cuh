@@ -50,18 +50,17 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                : "memory");
 }
 
-// Test the phase; if it is not complete yet, the thread is parked (it issues
-// nothing) until the phase completes or about kSuspendHintNs pass.
-constexpr uint32_t kSuspendHintNs = 1000000;   // 1 ms
-
+// Test the phase; if it is not complete yet, the thread may be parked for a
+// short, hardware-chosen time before the call returns false.  (An explicit
+// suspend-time hint made woken waiters noticeably late.)
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendHintNs)
+      : "r"(smem_u32(bar)), "r"(parity)
       : "memory");
   return ok != 0;
 }

@@ -29,77 +29,89 @@ __device__ __forceinline__ unsigned row_group_mask() {
 }
 
 // ---------------------------------------------------------------- ring_kv_write
-// Block = T tokens x {K, V} x H heads x L lanes (thread order: token, kv,
-// head, lane), so the threads of one (token, kv) cover that token's H*D bf16
-// contiguously.  A K thread reads the cos/sin of its own 8 pairs (the token's
-// table row is shared by all heads through L1); there is no block barrier.
+// Block = T tokens x H heads x L lanes (thread order: token, head, lane); a
+// thread owns 16 channels of one (token, head) and writes both its K and its
+// V codes, so the threads of one token cover that token's H*D bf16 of K and
+// of V contiguously.  The inputs, positions and cos/sin are loaded before
+// anything is read from the ring.  Thread 0 reads the write position once for
+// the block; as soon as it has, the block counts itself in, and the last
+// block to do so advances the ring state (every block has read the position
+// by then).  No barrier waits for the stores.
 template <int L>
-__global__ void __launch_bounds__(1024) ring_kv_write_kernel(RingView rv, const uint4* __restrict__ k,
-                                                             const uint4* __restrict__ v,
-                                                             const int32_t* __restrict__ pos, int n_new, int T) {
+__global__ void __launch_bounds__(512, 2) ring_kv_write_kernel(RingView rv, const uint4* __restrict__ k,
+                                                               const uint4* __restrict__ v,
+                                                               const int32_t* __restrict__ pos, int n_new, int T) {
   constexpr int D = L * 16;
+  __shared__ int wp_s;
   const int H = rv.H;
-  const int t0 = blockIdx.x * T;
-  const int wp = rv.state[ST_WP];
-
-  // This thread's 32 bytes of K or V go out first: they depend on nothing
-  // below, and the table gather and the barrier would otherwise delay them.
-  const int per_tok = 2 * H * L;
+  const int per_tok = H * L;
   const int tl = threadIdx.x / per_tok;
   const int rem = threadIdx.x - tl * per_tok;
-  const int kv = rem / (H * L);
-  const int h = (rem / L) % H;
+  const int h = rem / L;
   const int lane = rem % L;
-  const int tok = t0 + tl;
-  uint4 a = make_uint4(0, 0, 0, 0), b = a;
-  if (tok < n_new) {
-    const uint4* src = (kv ? v : k) + ((size_t)tok * H + h) * (D / 8) + lane * 2;
-    a = __ldg(src);
-    b = __ldg(src + 1);
-  }
+  const int tok = blockIdx.x * T + tl;
+  const bool live = tok < n_new;   // uniform over the L lanes of a row
 
+  uint4 ka = make_uint4(0, 0, 0, 0), kb = ka, va = ka, vb = ka;
+  if (live) {
+    const size_t off = ((size_t)tok * H + h) * (D / 8) + lane * 2;
+    ka = __ldg(k + off);
+    kb = __ldg(k + off + 1);
+    va = __ldg(v + off);
+    vb = __ldg(v + off + 1);
+  }
   bool bad = false;
   float2 cs[8];
-  if (kv == 0 && tok < n_new) {
+  if (live) {
     const int32_t* pr = pos + (size_t)tok * rv.n_axes;
 #pragma unroll
     for (int m = 0; m < 8; ++m) cs[m] = rope_cs(rv, pr, lane * 8 + m, bad);
   }
   if (bad) atomicOr(&rv.state[ST_ERR], DEVERR_POS_RANGE);
 
-  if (tok < n_new) {  // uniform over the L lanes of a row
-    float x[16];
-    bf16x8_to_f32(a, x);
-    bf16x8_to_f32(b, x + 8);
-    if (kv == 0) {
-#pragma unroll
-      for (int m = 0; m < 8; ++m) rope_pair(x[2 * m], x[2 * m + 1], cs[m].x, cs[m].y);
-    }
-    float amax = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
-    amax = row_max<L>(amax, row_group_mask<L>());
-    float scale, inv;
-    absmax_scale(amax, scale, inv);
-    const uint4 codes = quant16(x, inv);
-    const int slot = (int)(((long long)wp + tok) % rv.S);
-    uint8_t* dst = (kv ? rv.v_codes : rv.k_codes) + ((size_t)h * rv.S + slot) * D + lane * 16;
-    *reinterpret_cast<uint4*>(dst) = codes;
-    if (lane == 0) (kv ? rv.v_scale : rv.k_scale)[(size_t)h * rv.S_pad + slot] = scale;
-  }
-
-  // The last block to finish advances the ring state.  Every block read wp
-  // before arriving here, so the update cannot race with a reader.
+  if (threadIdx.x == 0) wp_s = rv.state[ST_WP];
   __syncthreads();
+  const int wp = wp_s;
   if (threadIdx.x == 0) {
-    __threadfence();
     const int done = atomicAdd(&rv.state[ST_DONE], 1);
     if (done == (int)gridDim.x - 1) {
       rv.state[ST_WP] = (int)(((long long)wp + n_new) % rv.S);
       rv.state[ST_NVALID] = min(rv.state[ST_NVALID] + n_new, rv.S);
       rv.state[ST_DONE] = 0;
-      __threadfence();
     }
+  }
+  if (!live) return;
+
+  const int slot = (int)(((long long)wp + tok) % rv.S);
+  const size_t row = (size_t)h * rv.S + slot;
+  const unsigned gm = row_group_mask<L>();
+  {
+    float x[16];
+    bf16x8_to_f32(ka, x);
+    bf16x8_to_f32(kb, x + 8);
+#pragma unroll
+    for (int m = 0; m < 8; ++m) rope_pair(x[2 * m], x[2 * m + 1], cs[m].x, cs[m].y);
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
+    amax = row_max<L>(amax, gm);
+    float scale, inv;
+    absmax_scale(amax, scale, inv);
+    *reinterpret_cast<uint4*>(rv.k_codes + row * D + lane * 16) = quant16(x, inv);
+    if (lane == 0) rv.k_scale[(size_t)h * rv.S_pad + slot] = scale;
+  }
+  {
+    float x[16];
+    bf16x8_to_f32(va, x);
+    bf16x8_to_f32(vb, x + 8);
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
+    amax = row_max<L>(amax, gm);
+    float scale, inv;
+    absmax_scale(amax, scale, inv);
+    *reinterpret_cast<uint4*>(rv.v_codes + row * D + lane * 16) = quant16(x, inv);
+    if (lane == 0) rv.v_scale[(size_t)h * rv.S_pad + slot] = scale;
   }
 }
 
@@ -144,10 +156,12 @@ __global__ void __launch_bounds__(256) q_prep_kernel(RingView rv, const uint4* _
 }
 
 // ---------------------------------------------------------------- delta_rerotate
-// One thread per 16 codes of a key row, over rows (head, slot) with
-// slot < n_valid.  In place: dequantise (code * scale, fp32), rotate the
-// temporal pairs by the host-computed (cos, sin) of -d * omega_j, re-quantise
-// with a fresh absmax scale.
+// In place over the key rows (head, slot) with slot < n_valid: dequantise
+// (code * scale, fp32), rotate the temporal pairs by the host-computed
+// (cos, sin) of -d * omega_j, re-quantise with a fresh absmax scale.  A row
+// is L lanes of 16 codes; the grid is sized to stay resident and each thread
+// walks rows with a stride of the whole grid, loading its next 16 codes and
+// scale before working on the current ones so that two loads are in flight.
 template <int L>
 __global__ void __launch_bounds__(256) delta_rerotate_kernel(RingView rv, DeltaTable dt) {
   constexpr int D = L * 16;
@@ -157,38 +171,63 @@ __global__ void __launch_bounds__(256) delta_rerotate_kernel(RingView rv, DeltaT
   if (threadIdx.x < 64) cs_s[threadIdx.x] = dt.cs[threadIdx.x];
   __syncthreads();
   const int n_valid = rv.state[ST_NVALID];
-  const long long gt = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  const long long row = gt / L;
-  const int lane = (int)(gt % L);
-  if (row >= (long long)rv.H * rv.S) return;  // whole rows
-  const int h = (int)(row / rv.S);
-  const int slot = (int)(row % rv.S);
-  if (slot >= n_valid) return;                // whole rows
-  uint8_t* p = rv.k_codes + ((size_t)h * rv.S + slot) * D + lane * 16;
-  float* sp = rv.k_scale + (size_t)h * rv.S_pad + slot;
-  const uint4 c = *reinterpret_cast<const uint4*>(p);
-  const float scale = *sp;
-  float x[16];
-  dequant16_codes(c, x);
+  if (n_valid <= 0) return;
+  const int chunks = rv.H * n_valid * L;          // <= 128 heads x 2^20 slots x 8
+  const int stride = gridDim.x * blockDim.x;      // a multiple of 32: rows never split
+  const int lane = threadIdx.x % L;
+  // pairs past the temporal axis are left as they are (not rotated by the
+  // identity, which would turn a -0 into +0)
+  float2 cs[8];
 #pragma unroll
-  for (int i = 0; i < 16; ++i) x[i] = __fmul_rn(x[i], scale);
-#pragma unroll
-  for (int m = 0; m < 8; ++m) {
-    const int pr = lane * 8 + m;
-    if (pr < dt.n_pairs) {
-      const float2 c = cs_s[pr];
-      rope_pair(x[2 * m], x[2 * m + 1], c.x, c.y);
+  for (int m = 0; m < 8; ++m) cs[m] = cs_s[(lane * 8 + m) & 63];
+  auto locate = [&](int c, uint8_t*& p, float*& sp) {
+    const int row = c / L;
+    const int h = row / n_valid;
+    const int slot = row - h * n_valid;
+    p = rv.k_codes + ((size_t)h * rv.S + slot) * D + lane * 16;
+    sp = rv.k_scale + (size_t)h * rv.S_pad + slot;
+  };
+  int c = blockIdx.x * blockDim.x + threadIdx.x;
+  if (c >= chunks) return;   // whole rows
+  uint8_t* p;
+  float* sp;
+  locate(c, p, sp);
+  uint4 code = *reinterpret_cast<const uint4*>(p);
+  float scale = *sp;
+  while (true) {
+    const int cn = c + stride;
+    const bool more = cn < chunks;   // whole rows
+    uint8_t* pn = p;
+    float* spn = sp;
+    uint4 code_n = code;
+    float scale_n = scale;
+    if (more) {
+      locate(cn, pn, spn);
+      code_n = *reinterpret_cast<const uint4*>(pn);
+      scale_n = *spn;
     }
-  }
-  float amax = 0.0f;
+    float x[16];
+    dequant16_codes(code, x);
 #pragma unroll
-  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
-  const unsigned mask = __activemask();
-  amax = row_max<L>(amax, mask & row_group_mask<L>());
-  float nscale, inv;
-  absmax_scale(amax, nscale, inv);
-  *reinterpret_cast<uint4*>(p) = quant16(x, inv);
-  if (lane == 0) *sp = nscale;
+    for (int i = 0; i < 16; ++i) x[i] = __fmul_rn(x[i], scale);
+#pragma unroll
+    for (int m = 0; m < 8; ++m)
+      if (lane * 8 + m < dt.n_pairs) rope_pair(x[2 * m], x[2 * m + 1], cs[m].x, cs[m].y);
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
+    amax = row_max<L>(amax, __activemask() & row_group_mask<L>());
+    float nscale, inv;
+    absmax_scale(amax, nscale, inv);
+    *reinterpret_cast<uint4*>(p) = quant16(x, inv);
+    if (lane == 0) *sp = nscale;
+    if (!more) break;
+    c = cn;
+    p = pn;
+    sp = spn;
+    code = code_n;
+    scale = scale_n;
+  }
 }
 
 // ---------------------------------------------------------------- debug quantiser
@@ -224,8 +263,8 @@ __global__ void __launch_bounds__(256) debug_quantize_kernel(const float* __rest
 template <int L>
 static cudaError_t launch_write_t(const RingView& rv, const void* k, const void* v, const int32_t* pos, int n_new,
                                   cudaStream_t st) {
-  const int per_tok = 2 * rv.H * L;
-  int T = 256 / per_tok;
+  const int per_tok = rv.H * L;
+  int T = 192 / per_tok;
   if (T < 1) T = 1;
   const int threads = per_tok * T;
   const int blocks = (n_new + T - 1) / T;
@@ -251,10 +290,29 @@ cudaError_t launch_q_prep(const RingView& rv, const void* q, const int32_t* q_po
   return cudaGetLastError();
 }
 
+// Blocks that stay resident on every SM at once (computed once per process).
+template <int L>
+static int rerotate_grid() {
+  static int blocks = 0;
+  if (blocks == 0) {
+    int dev = 0, sms = 0, per_sm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, delta_rerotate_kernel<L>, 256, 0) != cudaSuccess ||
+        sms <= 0 || per_sm <= 0)
+      return 0;
+    blocks = sms * per_sm;
+  }
+  return blocks;
+}
+
 cudaError_t launch_delta_rerotate(const RingView& rv, const DeltaTable& dt, cudaStream_t st) {
   const int L = rv.D / 16;
-  const long long threads = (long long)rv.H * rv.S * L;
-  const unsigned blocks = (unsigned)((threads + 255) / 256);
+  // enough threads for one pass over a full ring, at most what stays resident
+  const long long need = ((long long)rv.H * rv.S * L + 255) / 256;
+  const int resident = L == 4 ? rerotate_grid<4>() : rerotate_grid<8>();
+  if (resident <= 0) return cudaErrorInvalidConfiguration;
+  const unsigned blocks = (unsigned)(need < resident ? need : resident);
   if (L == 4)
     delta_rerotate_kernel<4><<<blocks, 256, 0, st>>>(rv, dt);
   else

@@ -36,6 +36,9 @@
 //               quarter w%4; finally the output, half of the columns each
 //   warps 8-11  the per-head fp16 range factor, then the per-tile widening
 //               of V to fp16 (one warp per SM sub-partition)
+// The softmax and MMA warps poll their barriers; the TMA and widening warps,
+// whose work runs ahead of need, park while they wait so that their polling
+// does not take issue slots from the softmax warps beside them.
 //   warp 12     TMA producer (the e4m3 query tile, then K, V codes into 4
 //               stages and their scales into 8)
 //   warp 13     TMEM allocation and MMA issue
@@ -452,9 +455,9 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
     for (int u = 0; u < T; ++u) {
       const int st = u % NSTAGE;
       const int b = u & 1;
-      if (!mbar_wait(&kv_full[st], (u / NSTAGE) & 1, abort_flag)) break;
+      if (!mbar_wait<true>(&kv_full[st], (u / NSTAGE) & 1, abort_flag)) break;
       // fp16 V buffer b is free once PV_{u-2} is done
-      if (u >= 2 && !mbar_wait(&pv_done[b], ((u - 2) >> 1) & 1, abort_flag)) break;
+      if (u >= 2 && !mbar_wait<true>(&pv_done[b], ((u - 2) >> 1) & 1, abort_flag)) break;
       const uint8_t* vsrc = sm + LY::V0 + st * BN * D;
       uint8_t* vdst = sm + LY::VH0 + b * BN * D * 2;
       // eight consecutive threads take the same chunk of eight consecutive
@@ -497,11 +500,11 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       for (int u = 0; u < T; ++u) {
         const int st = u % NSTAGE;
         const int sc = u % NSC;
-        if (u >= NSTAGE && !mbar_wait(&kv_empty[st], ((u / NSTAGE) - 1) & 1, abort_flag)) break;
+        if (u >= NSTAGE && !mbar_wait<true>(&kv_empty[st], ((u / NSTAGE) - 1) & 1, abort_flag)) break;
         mbar_arrive_expect_tx(&kv_full[st], 2 * BN * D);
         tma_load_3d(sm + LY::K0 + st * BN * D, &tmK, &kv_full[st], 0, u * BN, h);
         tma_load_3d(sm + LY::V0 + st * BN * D, &tmV, &kv_full[st], 0, u * BN, h);
-        if (u >= NSC && !mbar_wait(&sc_empty[sc], ((u / NSC) - 1) & 1, abort_flag)) break;
+        if (u >= NSC && !mbar_wait<true>(&sc_empty[sc], ((u / NSC) - 1) & 1, abort_flag)) break;
         mbar_arrive_expect_tx(&sc_full[sc], 2 * BN * 4);
         tma_load_2d(sm + LY::SC0 + sc * 2 * BN * 4, &tmSK, &sc_full[sc], u * BN, h);
         tma_load_2d(sm + LY::SC0 + sc * 2 * BN * 4 + BN * 4, &tmSV, &sc_full[sc], u * BN, h);

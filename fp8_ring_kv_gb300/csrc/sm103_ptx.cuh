@@ -51,8 +51,7 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
 }
 
 // Test the phase; if it is not complete yet, the thread may be parked for a
-// short, hardware-chosen time before the call returns false.  (An explicit
-// suspend-time hint made woken waiters noticeably late.)
+// short, hardware-chosen time before the call returns false.
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -61,6 +60,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
       : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// The same, but parked until the phase completes or about kSuspendHintNs
+// pass: for waiters off the critical path, so that their polling leaves the
+// issue slots to the warps that share their SM sub-partition.
+constexpr uint32_t kSuspendHintNs = 20000;   // 20 us
+__device__ __forceinline__ bool mbar_try_wait_parked(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendHintNs)
       : "memory");
   return ok != 0;
 }
@@ -81,13 +96,15 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
 // Wait for the phase with the given parity to complete.  Returns false (and
 // stops waiting) once ``*abort`` becomes non-zero or the time limit passes;
 // in the latter case it raises ``*abort`` itself so every other role of the
-// block stops waiting too.
+// block stops waiting too.  kParked: see mbar_try_wait_parked.
+template <bool kParked = false>
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
-  if (mbar_try_wait(bar, parity)) return true;
+  auto probe = [&]() { return kParked ? mbar_try_wait_parked(bar, parity) : mbar_try_wait(bar, parity); };
+  if (probe()) return true;
   const unsigned long long t0 = globaltimer_ns();
   uint32_t spins = 0;
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (probe()) return true;
     if ((++spins & 7u) == 0) {
       if (*abort) return false;
       if (globaltimer_ns() - t0 > kWaitLimitNs) {

@@ -1,0 +1,56 @@
+"""bench.py's multi-rank bookkeeping on CPU: two gloo ranks, the slowest
+rank's time taken for the whole job, throughput summed over the ranks."""
+import os
+import socket
+import sys
+
+import pytest
+import torch
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank(rank, world, port, q):
+    sys.path.insert(0, ROOT)
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world),
+                      LOCAL_RANK=str(rank))
+    import bench
+    r, w, lr = bench.dist_env()
+    bench.dist_init(w, "gloo")
+    bench.barrier(w)
+    # rank r "took" 1 + r seconds for 100 steps
+    t = bench.max_over_ranks(1.0 + r, w)
+    value = bench.aggregate(100, t, w)
+    q.put((r, w, lr, t, value))
+    torch.distributed.destroy_process_group()
+
+
+def test_two_ranks_take_the_slowest_time_and_sum_the_steps():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+    assert all(p.exitcode == 0 for p in procs)
+    got = sorted(q.get(timeout=10) for _ in range(2))
+    for r, (rank, world, local_rank, t, value) in enumerate(got):
+        assert (rank, world, local_rank) == (r, 2, r)
+        assert t == 2.0                       # the slower rank's time
+        assert value == pytest.approx(100 * 2 / 2.0)
+
+
+def test_single_rank_needs_no_process_group():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.max_over_ranks(3.5, 1) == 3.5
+    assert bench.aggregate(10, 2.0, 1) == 5.0

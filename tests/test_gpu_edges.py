@@ -40,7 +40,8 @@ def test_debug_quantize_bit_exact(d):
     scales = torch.empty(rows, dtype=torch.float32, device="cuda")
     K.kvring_debug_quantize(xd, rows, d, codes, scales)
     torch.cuda.synchronize()
-    want_c, want_s = quant.quantize_rows(x)
+    with np.errstate(over="ignore"):   # 448 / amax overflows to inf on the subnormal row, as in fp32
+        want_c, want_s = quant.quantize_rows(x)
     got_c, got_s = codes.cpu().numpy(), scales.cpu().numpy()
     bad = np.argwhere(got_c != want_c)
     assert bad.size == 0, f"codes differ at {len(bad)} places, first {bad[:5].tolist()}"

@@ -119,18 +119,20 @@ __global__ void __launch_bounds__(512, 2) ring_kv_write_kernel(RingView rv, cons
 // The queries of one attention call: RoPE in fp32 at their positions and
 // e4m3 with one absmax scale per (query, head), into the workspace's query
 // scratch (codes [n_q][H][D], scales [H][Q_pad]) that the attention kernel
-// then loads by TMA.  Same thread layout and arithmetic as the K side of
-// ring_kv_write.
+// then loads by TMA.  Same thread layout (T queries x H heads x L lanes per
+// block) and arithmetic as the K side of ring_kv_write.
 template <int L>
-__global__ void __launch_bounds__(256) q_prep_kernel(RingView rv, const uint4* __restrict__ q,
-                                                     const int32_t* __restrict__ pos, int n_q) {
+__global__ void __launch_bounds__(512, 2) q_prep_kernel(RingView rv, const uint4* __restrict__ q,
+                                                        const int32_t* __restrict__ pos, int n_q, int T) {
   constexpr int D = L * 16;
-  const long long gt = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  const long long row = gt / L;            // = query * H + head
-  const int lane = (int)(gt % L);
-  if (row >= (long long)n_q * rv.H) return;  // whole rows
-  const int qi = (int)(row / rv.H);
-  const int h = (int)(row % rv.H);
+  const int per_q = rv.H * L;
+  const int tl = threadIdx.x / per_q;
+  const int rem = threadIdx.x - tl * per_q;
+  const int h = rem / L;
+  const int lane = rem % L;
+  const int qi = blockIdx.x * T + tl;
+  if (qi >= n_q) return;   // whole rows
+  const size_t row = (size_t)qi * rv.H + h;
   const uint4* src = q + row * (D / 8) + lane * 2;
   const uint4 a = __ldg(src);
   const uint4 b = __ldg(src + 1);
@@ -148,7 +150,7 @@ __global__ void __launch_bounds__(256) q_prep_kernel(RingView rv, const uint4* _
   float amax = 0.0f;
 #pragma unroll
   for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
-  amax = row_max<L>(amax, __activemask() & row_group_mask<L>());
+  amax = row_max<L>(amax, row_group_mask<L>());
   float scale, inv;
   absmax_scale(amax, scale, inv);
   *reinterpret_cast<uint4*>(rv.q_codes + row * D + lane * 16) = quant16(x, inv);
@@ -180,18 +182,22 @@ __global__ void __launch_bounds__(256) delta_rerotate_kernel(RingView rv, DeltaT
   float2 cs[8];
 #pragma unroll
   for (int m = 0; m < 8; ++m) cs[m] = cs_s[(lane * 8 + m) & 63];
-  auto locate = [&](int c, uint8_t*& p, float*& sp) {
-    const int row = c / L;
-    const int h = row / n_valid;
-    const int slot = row - h * n_valid;
-    p = rv.k_codes + ((size_t)h * rv.S + slot) * D + lane * 16;
-    sp = rv.k_scale + (size_t)h * rv.S_pad + slot;
-  };
+  // the thread's row (head h, slot) advances by a fixed number of rows per
+  // step: kept as (h, slot) and carried, instead of two divisions per row
+  const int row_step = stride / L;
+  const int step_h = row_step / n_valid;
+  const int step_slot = row_step - step_h * n_valid;
   int c = blockIdx.x * blockDim.x + threadIdx.x;
   if (c >= chunks) return;   // whole rows
+  int h = (c / L) / n_valid;
+  int slot = c / L - h * n_valid;
+  auto locate = [&](int hh, int ss, uint8_t*& p, float*& sp) {
+    p = rv.k_codes + ((size_t)hh * rv.S + ss) * D + lane * 16;
+    sp = rv.k_scale + (size_t)hh * rv.S_pad + ss;
+  };
   uint8_t* p;
   float* sp;
-  locate(c, p, sp);
+  locate(h, slot, p, sp);
   uint4 code = *reinterpret_cast<const uint4*>(p);
   float scale = *sp;
   while (true) {
@@ -201,8 +207,13 @@ __global__ void __launch_bounds__(256) delta_rerotate_kernel(RingView rv, DeltaT
     float* spn = sp;
     uint4 code_n = code;
     float scale_n = scale;
+    int hn = h + step_h, sn = slot + step_slot;
+    if (sn >= n_valid) {
+      sn -= n_valid;
+      ++hn;
+    }
     if (more) {
-      locate(cn, pn, spn);
+      locate(hn, sn, pn, spn);
       code_n = *reinterpret_cast<const uint4*>(pn);
       scale_n = *spn;
     }
@@ -223,6 +234,8 @@ __global__ void __launch_bounds__(256) delta_rerotate_kernel(RingView rv, DeltaT
     if (lane == 0) *sp = nscale;
     if (!more) break;
     c = cn;
+    h = hn;
+    slot = sn;
     p = pn;
     sp = spn;
     code = code_n;
@@ -281,12 +294,14 @@ cudaError_t launch_ring_kv_write(const RingView& rv, const void* k, const void* 
 
 cudaError_t launch_q_prep(const RingView& rv, const void* q, const int32_t* q_pos, int n_q, cudaStream_t st) {
   const int L = rv.D / 16;
-  const long long threads = (long long)n_q * rv.H * L;
-  const unsigned blocks = (unsigned)((threads + 255) / 256);
+  const int per_q = rv.H * L;
+  int T = 192 / per_q;
+  if (T < 1) T = 1;
+  const int blocks = (n_q + T - 1) / T;
   if (L == 4)
-    q_prep_kernel<4><<<blocks, 256, 0, st>>>(rv, static_cast<const uint4*>(q), q_pos, n_q);
+    q_prep_kernel<4><<<blocks, per_q * T, 0, st>>>(rv, static_cast<const uint4*>(q), q_pos, n_q, T);
   else
-    q_prep_kernel<8><<<blocks, 256, 0, st>>>(rv, static_cast<const uint4*>(q), q_pos, n_q);
+    q_prep_kernel<8><<<blocks, per_q * T, 0, st>>>(rv, static_cast<const uint4*>(q), q_pos, n_q, T);
   return cudaGetLastError();
 }
 

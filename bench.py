@@ -54,6 +54,10 @@ ATTN_FLOPS = 4 * N * S * D * H                         # QK^T and PV
 # kernels per step: ring_kv_write, delta_rerotate, and the attend call's two
 # (query RoPE + e4m3, then fp8_ring_attn)
 KERNELS_PER_STEP = 4
+# DRAM bytes (read + write) of one fp8_ring_attn launch at this workload, from
+# one ncu capture (profiles/fp8_ring_attn_single_call.md); set to None when
+# the kernel changes until it is captured again
+ATTN_DRAM_BYTES = 39_150_592 + 4_608
 
 
 # ---------------------------------------------------------------- distributed helpers
@@ -437,7 +441,7 @@ def main():
     if rank == 0:
         att = res["kernels"]["fp8_ring_attn"]
         roof = {"bound": "tensor", "achieved": att["rate"], "peak": round(res["fp8_peak"], 1), "unit": "TFLOP/s",
-                "frac": att["frac_of_fp8"], "traffic": None,
+                "frac": att["frac_of_fp8"], "traffic": ATTN_DRAM_BYTES,
                 "peak_source": f"{res['peaks']['source']}: bf16 burst x 2 (nominal fp8/bf16 ratio)"}
         line = {
             "metric": METRIC, "value": round(res["value"], 2), "unit": "calls/s", "n_gpus": world,

@@ -151,13 +151,16 @@ def make_rings(n_rings, dev):
     rings, inputs = [], []
     kp, vp, pp = prefill.k.to(dev), prefill.v.to(dev), torch.from_numpy(prefill.pos).to(dev)
     pos = torch.from_numpy(synth.lin_pos(S, N)).to(dev)
+    # the single-call workload's recipe: the same 1% of the channels scaled x8
+    # in K, V and Q (the channels its own first draw picks)
+    ch = synth.outlier_channels(synth.rng(1), H, D)
     for r in range(n_rings):
         ring = KVRing.from_shape(shape, KVRING_OUT_BF16)
         ring.write(kp, vp, pp)
         g = synth.rng(1, 100 + r)
-        k = synth.normal_bf16(g, (N, H, D)).to(dev)
-        v = synth.normal_bf16(g, (N, H, D)).to(dev)
-        q = synth.normal_bf16(g, (N, H, D)).to(dev)
+        k = synth.normal_bf16(g, (N, H, D), ch).to(dev)
+        v = synth.normal_bf16(g, (N, H, D), ch).to(dev)
+        q = synth.normal_bf16(g, (N, H, D), ch).to(dev)
         out = torch.empty((N, H, D), dtype=torch.bfloat16, device=dev)
         rings.append(ring)
         inputs.append((k, v, q, pos, out))
@@ -328,9 +331,11 @@ class OracleSample:
         pre = list(synth.single().ops)[0]
         kp, vp = synth.to_f32(pre.k)[:, :heads], synth.to_f32(pre.v)[:, :heads]
         g = synth.rng(1, 100)
-        self.k = synth.to_f32(synth.normal_bf16(g, (N, heads, D)))[:self.n_w]
-        self.v = synth.to_f32(synth.normal_bf16(g, (N, heads, D)))[:self.n_w]
-        self.q = synth.to_f32(synth.normal_bf16(g, (N, heads, D)))
+        ch = synth.outlier_channels(synth.rng(1), H, D)
+        ch = ch[ch < heads * D]                        # those of the sampled heads
+        self.k = synth.to_f32(synth.normal_bf16(g, (N, heads, D), ch))[:self.n_w]
+        self.v = synth.to_f32(synth.normal_bf16(g, (N, heads, D), ch))[:self.n_w]
+        self.q = synth.to_f32(synth.normal_bf16(g, (N, heads, D), ch))
         self.pos = synth.lin_pos(S, N)
         self.ring = OracleRing(heads, D, S, (D,))
         self.ring.write(kp, vp, pre.pos)

@@ -14,7 +14,7 @@
 //   t    = S_j * s_k (per column);  logit*log2(e) = t * s_q * log2(e)/sqrt(D)
 //   online softmax in base 2: e = exp2(t*r - m + c), l += e, with a running
 //   row maximum m that is only raised (and O rescaled) when a tile's maximum
-//   exceeds it by more than 2^8, so e <= 2^8 * 2^c
+//   exceeds it by more than 2^14, so e <= 2^14 * 2^c
 //   P_j  = e * s_v (per column) rounded to fp16, in TMEM
 //   O   += P_j . Vcodes_j                  tcgen05 kind::f16 (A = P from TMEM)
 //   out  = O / l
@@ -64,7 +64,16 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TM_S = 0;      // S buffer b: fp32 [128 lanes][128] at columns 128 b
 constexpr uint32_t TM_P = 256;    // P buffer b: fp16 pairs [128 lanes][64] at columns 256 + 64 b
 constexpr uint32_t TM_O = 384;    // O: fp32 [128 lanes][D]
-constexpr float kLazyRescale = 8.0f;   // log2 of the largest unnormalised weight
+// log2 of the largest unnormalised weight.  A wide bound keeps the rescale
+// (which recomputes a tile) rare even when the logits of a row spread over
+// many octaves; fp16 P still has ~15 octaves below the row maximum before
+// its weights turn subnormal, far below what reaches the output.
+constexpr int kLazyLog2 = 14;
+constexpr float kLazyRescale = (float)kLazyLog2;
+// A running maximum is set this many octaves above the tile maximum that sets
+// it (weights then start at most 2^-4), so later tiles may exceed the observed
+// maximum by kLazyLog2 + 4 octaves before a rescale.
+constexpr float kHeadroom = 4.0f;
 
 template <int D>
 struct AttnLayout {
@@ -274,8 +283,8 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
           mb = fmaxf(mb, __shfl_xor_sync(0xFFFFFFFFu, mb, 2));
           const bool grow0 = j == 0 || ma > m_run[0] + kLazyRescale;
           const bool grow1 = j == 0 || mb > m_run[1] + kLazyRescale;
-          const float mn0 = grow0 ? fmaxf(m_run[0], ma) : m_run[0];
-          const float mn1 = grow1 ? fmaxf(m_run[1], mb) : m_run[1];
+          const float mn0 = grow0 ? fmaxf(m_run[0], ma + kHeadroom) : m_run[0];
+          const float mn1 = grow1 ? fmaxf(m_run[1], mb + kHeadroom) : m_run[1];
           if (j > 0) {
             // O holds rows weighted by exp2(-m_run): once PV_{j-1} (and so
             // every earlier PV) is done, bring them to exp2(-m_new)
@@ -440,9 +449,10 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       asm volatile("bar.sync 1, %0;" ::"n"(CONV_THREADS) : "memory");
       if (ct == 0) {
         const float m = __int_as_float(*maxsv_bits);
-        // weights reach 2^8 * 2^c; with c = 6 - floor(log2 max s_v) every
-        // P = weight * s_v stays below 2^15 (fp16 max 65504)
-        int c = m > 0.0f ? 6 - ilogbf(m) : 0;
+        // weights reach 2^kLazyLog2 * 2^c; with c = 14 - kLazyLog2 -
+        // floor(log2 max s_v) every P = weight * s_v stays below 2^15 (fp16
+        // max 65504)
+        int c = m > 0.0f ? 14 - kLazyLog2 - ilogbf(m) : 0;
         c = c < -64 ? -64 : (c > 64 ? 64 : c);
         *cv_smem = (float)c;
       }

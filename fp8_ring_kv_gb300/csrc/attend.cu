@@ -217,6 +217,38 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
     }
     bool ok = mbar_wait(q_full, 0, abort_flag);
     const float log2cv = *cv_smem;
+    // Raise the running maxima of rows a and b to mn0, mn1 at tile j > 0:
+    // O holds rows weighted by exp2(-m_run), so once PV_{j-1} (and so every
+    // earlier PV) is done they are brought to exp2(-m_new), with the sums.
+    // Returns the factors 2^(m_old - m_new); false if the wait gave up.
+    auto raise_max = [&](int j, float mn0, float mn1, float& al0, float& al1) -> bool {
+      al0 = 1.0f;
+      al1 = 1.0f;
+      if (j > 0) {
+        if (!mbar_wait(&pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag)) return false;
+        tc_fence_after();
+        al0 = ex2f(m_run[0] - mn0);
+        al1 = ex2f(m_run[1] - mn1);
+#pragma unroll 1
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t o[16];
+          tmem_ld_16x256b_x4(o_addr + c0, o);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            o[4 * k] = __float_as_uint(__uint_as_float(o[4 * k]) * al0);
+            o[4 * k + 1] = __float_as_uint(__uint_as_float(o[4 * k + 1]) * al0);
+            o[4 * k + 2] = __float_as_uint(__uint_as_float(o[4 * k + 2]) * al1);
+            o[4 * k + 3] = __float_as_uint(__uint_as_float(o[4 * k + 3]) * al1);
+          }
+          tmem_st_16x256b_x4(o_addr + c0, o);
+        }
+        lsum[0] = mul2(lsum[0], make_float2(al0, al0));
+        lsum[1] = mul2(lsum[1], make_float2(al1, al1));
+      }
+      m_run[0] = mn0;
+      m_run[1] = mn1;
+      return true;
+    };
     for (int j = 0; ok && j < T; ++j) {
       const int b = j & 1;
       const int sc = j % NSC;
@@ -285,34 +317,11 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
           const bool grow1 = j == 0 || mb > m_run[1] + kLazyRescale;
           const float mn0 = grow0 ? fmaxf(m_run[0], ma + kHeadroom) : m_run[0];
           const float mn1 = grow1 ? fmaxf(m_run[1], mb + kHeadroom) : m_run[1];
-          if (j > 0) {
-            // O holds rows weighted by exp2(-m_run): once PV_{j-1} (and so
-            // every earlier PV) is done, bring them to exp2(-m_new)
-            if (!mbar_wait(&pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const float al0 = ex2f(m_run[0] - mn0);
-            const float al1 = ex2f(m_run[1] - mn1);
-#pragma unroll 1
-            for (int c0 = 0; c0 < D; c0 += 32) {
-              uint32_t o[16];
-              tmem_ld_16x256b_x4(o_addr + c0, o);
-#pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                o[4 * k] = __float_as_uint(__uint_as_float(o[4 * k]) * al0);
-                o[4 * k + 1] = __float_as_uint(__uint_as_float(o[4 * k + 1]) * al0);
-                o[4 * k + 2] = __float_as_uint(__uint_as_float(o[4 * k + 2]) * al1);
-                o[4 * k + 3] = __float_as_uint(__uint_as_float(o[4 * k + 3]) * al1);
-              }
-              tmem_st_16x256b_x4(o_addr + c0, o);
-            }
-            lsum[0] = mul2(lsum[0], make_float2(al0, al0));
-            lsum[1] = mul2(lsum[1], make_float2(al1, al1));
+          float al0, al1;
+          if (!raise_max(j, mn0, mn1, al0, al1)) {
+            ok = false;
+            break;
           }
-          m_run[0] = mn0;
-          m_run[1] = mn1;
         }
         // weights e = exp2(t * rq + c - m), P = e * s_v in fp16 pairs; the
         // pair of row a at repetition k goes to P column 4k + t%4 of row a
@@ -331,6 +340,38 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         }
 #pragma unroll
         for (int i = 0; i < 64; ++i) x[i] = ex2f(x[i]);
+        // A row whose tile maximum passed the bound (decided only now, so that
+        // the maxima overlap the exponentials): raise its maximum and scale the
+        // weights just computed, in fp32, by 2^(m_old - m_new) -- the same as
+        // recomputing them up to rounding -- unless one of them overflowed,
+        // in which case the tile is recomputed from S (pass 1).
+        if (pass == 0 && __any_sync(0xFFFFFFFFu, ma > m_run[0] + kLazyRescale || mb > m_run[1] + kLazyRescale)) {
+          ma = fmaxf(ma, __shfl_xor_sync(0xFFFFFFFFu, ma, 1));
+          mb = fmaxf(mb, __shfl_xor_sync(0xFFFFFFFFu, mb, 1));
+          ma = fmaxf(ma, __shfl_xor_sync(0xFFFFFFFFu, ma, 2));
+          mb = fmaxf(mb, __shfl_xor_sync(0xFFFFFFFFu, mb, 2));
+          bool finite = true;
+#pragma unroll
+          for (int i = 0; i < 64; ++i) finite = finite && x[i] < INFINITY;
+          if (!__all_sync(0xFFFFFFFFu, finite)) continue;   // -> pass 1
+          const float mn0 = ma > m_run[0] + kLazyRescale ? ma + kHeadroom : m_run[0];
+          const float mn1 = mb > m_run[1] + kLazyRescale ? mb + kHeadroom : m_run[1];
+          float al0, al1;
+          if (!raise_max(j, mn0, mn1, al0, al1)) {
+            ok = false;
+            break;
+          }
+          const float2 fa = make_float2(al0, al0), fb = make_float2(al1, al1);
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            const float2 ea = mul2(make_float2(x[4 * k], x[4 * k + 1]), fa);
+            const float2 eb = mul2(make_float2(x[4 * k + 2], x[4 * k + 3]), fb);
+            x[4 * k] = ea.x;
+            x[4 * k + 1] = ea.y;
+            x[4 * k + 2] = eb.x;
+            x[4 * k + 3] = eb.y;
+          }
+        }
         float2 la0 = make_float2(0.0f, 0.0f), la1 = la0, lb0 = la0, lb1 = la0;
 #pragma unroll
         for (int k = 0; k < 16; k += 2) {
@@ -349,9 +390,6 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
           pk[2 * k] = cvt_f16x2(pa2.x, pa2.y);
           pk[2 * k + 1] = cvt_f16x2(pb2.x, pb2.y);
         }
-        // decided only now, so that the maxima overlap the exponentials
-        if (pass == 0 && __any_sync(0xFFFFFFFFu, ma > m_run[0] + kLazyRescale || mb > m_run[1] + kLazyRescale))
-          continue;   // -> pass 1
         break;
       }
       if (!ok) break;

@@ -142,8 +142,6 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
   const int qt = blockIdx.x;
   const int h = blockIdx.y;
   const int H = rv.H;
-  const int n_valid = rv.state[ST_NVALID];
-  const int T = (n_valid + BN - 1) / BN;
 
   if (tid == 0) {
     for (int i = 0; i < NSTAGE; ++i) {
@@ -180,6 +178,12 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // the set-up above touches no global memory; the ring state, the cache and
+  // the query scratch come from earlier kernels
+  pdl_wait();
+  pdl_trigger();
+  const int n_valid = rv.state[ST_NVALID];
+  const int T = (n_valid + BN - 1) / BN;
 
   if (n_valid <= 0) {
     // nothing to attend to: zeros, and a flag the host can read
@@ -618,12 +622,10 @@ cudaError_t launch_fp8_ring_attn(const RingView& rv, const AttnMaps& maps, const
                                  int out_f32, cudaStream_t st) {
   const dim3 grid((n_q + BM - 1) / BM, rv.H);
   if (rv.D == 128)
-    fp8_ring_attn_kernel<128><<<grid, ATT_THREADS, AttnLayout<128>::ALLOC, st>>>(
-        maps.k_codes, maps.v_codes, maps.k_scale, maps.v_scale, tmQ, rv, n_q, out, out_f32);
-  else
-    fp8_ring_attn_kernel<64><<<grid, ATT_THREADS, AttnLayout<64>::ALLOC, st>>>(
-        maps.k_codes, maps.v_codes, maps.k_scale, maps.v_scale, tmQ, rv, n_q, out, out_f32);
-  return cudaGetLastError();
+    return launch_pdl(fp8_ring_attn_kernel<128>, grid, dim3(ATT_THREADS), AttnLayout<128>::ALLOC, st, maps.k_codes,
+                      maps.v_codes, maps.k_scale, maps.v_scale, tmQ, rv, n_q, out, out_f32);
+  return launch_pdl(fp8_ring_attn_kernel<64>, grid, dim3(ATT_THREADS), AttnLayout<64>::ALLOC, st, maps.k_codes,
+                    maps.v_codes, maps.k_scale, maps.v_scale, tmQ, rv, n_q, out, out_f32);
 }
 
 }  // namespace kvring_dev

@@ -51,6 +51,8 @@ __global__ void __launch_bounds__(512, 2) ring_kv_write_kernel(RingView rv, cons
   const int lane = rem % L;
   const int tok = blockIdx.x * T + tl;
   const bool live = tok < n_new;   // uniform over the L lanes of a row
+  pdl_wait();
+  pdl_trigger();
 
   uint4 ka = make_uint4(0, 0, 0, 0), kb = ka, va = ka, vb = ka;
   if (live) {
@@ -131,6 +133,8 @@ __global__ void __launch_bounds__(512, 2) q_prep_kernel(RingView rv, const uint4
   const int h = rem / L;
   const int lane = rem % L;
   const int qi = blockIdx.x * T + tl;
+  pdl_wait();
+  pdl_trigger();
   if (qi >= n_q) return;   // whole rows
   const size_t row = (size_t)qi * rv.H + h;
   const uint4* src = q + row * (D / 8) + lane * 2;
@@ -171,6 +175,8 @@ __global__ void __launch_bounds__(256) delta_rerotate_kernel(RingView rv, DeltaT
   // not from the parameter space (which would serialise them)
   __shared__ float2 cs_s[64];
   if (threadIdx.x < 64) cs_s[threadIdx.x] = dt.cs[threadIdx.x];
+  pdl_wait();
+  pdl_trigger();
   __syncthreads();
   const int n_valid = rv.state[ST_NVALID];
   if (n_valid <= 0) return;
@@ -281,9 +287,8 @@ static cudaError_t launch_write_t(const RingView& rv, const void* k, const void*
   if (T < 1) T = 1;
   const int threads = per_tok * T;
   const int blocks = (n_new + T - 1) / T;
-  ring_kv_write_kernel<L><<<blocks, threads, 0, st>>>(rv, static_cast<const uint4*>(k),
-                                                         static_cast<const uint4*>(v), pos, n_new, T);
-  return cudaGetLastError();
+  return launch_pdl(ring_kv_write_kernel<L>, dim3(blocks), dim3(threads), 0, st, rv, static_cast<const uint4*>(k),
+                    static_cast<const uint4*>(v), pos, n_new, T);
 }
 
 cudaError_t launch_ring_kv_write(const RingView& rv, const void* k, const void* v, const int32_t* pos, int n_new,
@@ -299,10 +304,10 @@ cudaError_t launch_q_prep(const RingView& rv, const void* q, const int32_t* q_po
   if (T < 1) T = 1;
   const int blocks = (n_q + T - 1) / T;
   if (L == 4)
-    q_prep_kernel<4><<<blocks, per_q * T, 0, st>>>(rv, static_cast<const uint4*>(q), q_pos, n_q, T);
-  else
-    q_prep_kernel<8><<<blocks, per_q * T, 0, st>>>(rv, static_cast<const uint4*>(q), q_pos, n_q, T);
-  return cudaGetLastError();
+    return launch_pdl(q_prep_kernel<4>, dim3(blocks), dim3(per_q * T), 0, st, rv, static_cast<const uint4*>(q),
+                      q_pos, n_q, T);
+  return launch_pdl(q_prep_kernel<8>, dim3(blocks), dim3(per_q * T), 0, st, rv, static_cast<const uint4*>(q), q_pos,
+                    n_q, T);
 }
 
 // Blocks that stay resident on every SM at once (computed once per process).
@@ -328,11 +333,8 @@ cudaError_t launch_delta_rerotate(const RingView& rv, const DeltaTable& dt, cuda
   const int resident = L == 4 ? rerotate_grid<4>() : rerotate_grid<8>();
   if (resident <= 0) return cudaErrorInvalidConfiguration;
   const unsigned blocks = (unsigned)(need < resident ? need : resident);
-  if (L == 4)
-    delta_rerotate_kernel<4><<<blocks, 256, 0, st>>>(rv, dt);
-  else
-    delta_rerotate_kernel<8><<<blocks, 256, 0, st>>>(rv, dt);
-  return cudaGetLastError();
+  if (L == 4) return launch_pdl(delta_rerotate_kernel<4>, dim3(blocks), dim3(256), 0, st, rv, dt);
+  return launch_pdl(delta_rerotate_kernel<8>, dim3(blocks), dim3(256), 0, st, rv, dt);
 }
 
 cudaError_t launch_debug_quantize(const float* x, long long rows, int d, uint8_t* codes, float* scales,

@@ -115,6 +115,15 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
+// ---------------------------------------------------------------- dependent launch
+// Kernels launched with programmatic stream serialisation may start while the
+// previous kernel of the stream is still running.  pdl_wait() returns once
+// that kernel (and so every earlier one) has completed and its writes are
+// visible; nothing in global memory is touched before it.  pdl_trigger()
+// then lets the next kernel of the stream start its own launch and set-up.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---------------------------------------------------------------- fences
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

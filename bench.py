@@ -57,7 +57,7 @@ KERNELS_PER_STEP = 4
 # DRAM bytes (read + write) of one fp8_ring_attn launch at this workload, from
 # one ncu capture (profiles/fp8_ring_attn_single_call.md); set to None when
 # the kernel changes until it is captured again
-ATTN_DRAM_BYTES = 39_150_592 + 4_608
+ATTN_DRAM_BYTES = 39_161_344 + 1_536
 
 
 # ---------------------------------------------------------------- distributed helpers

@@ -36,12 +36,12 @@
 //               quarter w%4; finally the output, half of the columns each
 //   warps 8-11  the per-head fp16 range factor, then the per-tile widening
 //               of V to fp16 (one warp per SM sub-partition)
-// The softmax and MMA warps poll their barriers; the TMA and widening warps,
-// whose work runs ahead of need, park while they wait so that their polling
-// does not take issue slots from the softmax warps beside them.
 //   warp 12     TMA producer (the e4m3 query tile, then K, V codes into 4
 //               stages and their scales into 8)
 //   warp 13     TMEM allocation and MMA issue
+// The softmax and MMA warps poll their barriers; the TMA and widening warps,
+// whose work runs ahead of need, park while they wait so that their polling
+// does not take issue slots from the softmax warps beside them.
 #include <cfloat>
 
 #include "common.cuh"
@@ -64,10 +64,10 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TM_S = 0;      // S buffer b: fp32 [128 lanes][128] at columns 128 b
 constexpr uint32_t TM_P = 256;    // P buffer b: fp16 pairs [128 lanes][64] at columns 256 + 64 b
 constexpr uint32_t TM_O = 384;    // O: fp32 [128 lanes][D]
-// log2 of the largest unnormalised weight.  A wide bound keeps the rescale
-// (which recomputes a tile) rare even when the logits of a row spread over
-// many octaves; fp16 P still has ~15 octaves below the row maximum before
-// its weights turn subnormal, far below what reaches the output.
+// log2 of the largest unnormalised weight.  A wide bound keeps rescales (a
+// wait for the previous PV, O and the sums rescaled) rare even when the
+// logits of a row spread over many octaves; P = weight * s_v * 2^c still fits
+// fp16 because the per-head factor 2^c shrinks by the same number of octaves.
 constexpr int kLazyLog2 = 14;
 constexpr float kLazyRescale = (float)kLazyLog2;
 // A running maximum is set this many octaves above the tile maximum that sets

@@ -7,9 +7,10 @@ no code, table or constant generator with the CUDA library; the two meet only
 through the seeded inputs of ``synth``.
 
 Source: "Runway Characters: Serving a 57B Video Diffusion Transformer for
-Real-Time Conversation" (arXiv:2611.05642), §4.1 (ring cache with a device-side
-write position), §4.2 (RoPE at write, delta rotation at reset), §4.3 (FP8 at
-write), Appendix G (cache update and position reset).
+Real-Time Conversation" (arXiv:2611.05642), Introduction ("The model": global
+slots and the window of six latent frames), §4.1 (ring cache with a
+device-side write position), §4.2 (RoPE at write, delta rotation at reset),
+§4.3 (FP8 at write), Appendix G (cache update and position reset).
 
 Every function is written from the plain definition of what it computes:
 
@@ -18,8 +19,9 @@ Every function is written from the plain definition of what it computes:
 * ``quant`` -- per-token-per-head absmax quantisation to e4m3.
 * ``rope``  -- RoPE frequencies, the fp32 cos/sin tables, RoPE in fp32 and in
   fp64, the delta rotation R(-d).
-* ``ring``  -- the ring of slots with its write position, and the whole call
-  sequence (write / reset_positions / attend).
+* ``ring``  -- the ring of slots with its write position, the optional global
+  slots ahead of it (written once, never rotated), and the whole call
+  sequence (write_global / write / reset_positions / attend).
 * ``attention`` -- dense softmax attention in fp64.
 
 Parity pins (tests/test_oracle_*.py) tie each function to something other than

@@ -19,6 +19,18 @@ n_valid <- min(n_valid + N, S).  Slots fill in order 0, 1, 2, ... so the valid
 slots are always 0 .. n_valid-1; attention is a sum over them and does not
 depend on their order.
 
+Global slots (Introduction, "The model"; Appendix G): a cache may hold
+``n_global`` = G slots written once per session, ahead of the window ring.
+Slots 0 .. G-1 are the globals; the window ring is slots G .. S-1 (W = S - G
+of them).  The globals are written by one call of exactly G tokens, before any
+window write; a window write of N tokens then puts token i into slot
+G + (wp + i) mod W, wp <- (wp + N) mod W and n_valid <- min(n_valid + N, S).
+A reset rotates the valid window slots G .. n_valid-1 only: the global
+tokens' positions do not depend on the window.  With G = 0 this is the plain
+ring above.  A ring of six latent frames (Appendix G) is the window ring with
+W = 6 x 757 and writes of 757 tokens: every frame then fills whole,
+consecutive slots and the seventh frame replaces the first.
+
 Scales are per (token, head), recomputed at write and at reset (absmax, see
 ``quant``); this replaces the paper's per-(layer, head) scales calibrated once
 per session.
@@ -30,10 +42,15 @@ from .attention import attend_f64
 
 
 class OracleRing:
-    def __init__(self, heads, head_dim, n_slots, axis_dims, base=10000.0):
+    def __init__(self, heads, head_dim, n_slots, axis_dims, base=10000.0, n_global=0):
         if sum(axis_dims) != head_dim or any(d % 2 for d in axis_dims):
             raise ValueError("axis_dims must be even and sum to head_dim")
         self.H, self.D, self.S = int(heads), int(head_dim), int(n_slots)
+        self.G = int(n_global)
+        if not 0 <= self.G < self.S:
+            raise ValueError("n_global must leave at least one window slot")
+        self.W = self.S - self.G
+        self.globals_written = False
         self.axis_dims = tuple(int(d) for d in axis_dims)
         self.base = float(base)
         self.k_codes = np.zeros((self.H, self.S, self.D), np.uint8)
@@ -45,40 +62,62 @@ class OracleRing:
 
     # -- write ---------------------------------------------------------------
     def slots_for(self, n_new):
-        return (self.wp + np.arange(n_new)) % self.S
+        return self.G + (self.wp + np.arange(n_new)) % self.W
 
-    def write(self, k, v, pos):
-        """k, v: float32 [N, H, D] (bf16 values); pos: int [N, n_axes].
-        Returns the slot index of each token."""
-        k = np.asarray(k, np.float32)
-        v = np.asarray(v, np.float32)
-        n = k.shape[0]
-        if not 1 <= n <= self.S:
-            raise ValueError("a write must carry 1 .. n_slots tokens")
+    def _store(self, k, v, pos, slots):
+        """RoPE on K (fp32), absmax e4m3 of K and V, into ``slots``."""
         kc, ks = quant.quantize_rows(rope.rope_f32(k, pos, self.axis_dims, self.base))
         vc, vs = quant.quantize_rows(v)
-        slots = self.slots_for(n)
         self.k_codes[:, slots, :] = np.transpose(kc, (1, 0, 2))
         self.v_codes[:, slots, :] = np.transpose(vc, (1, 0, 2))
         self.k_scale[:, slots] = ks.T
         self.v_scale[:, slots] = vs.T
-        self.wp = int((self.wp + n) % self.S)
+
+    def write(self, k, v, pos):
+        """k, v: float32 [N, H, D] (bf16 values); pos: int [N, n_axes].
+        Window write.  Returns the slot index of each token."""
+        k = np.asarray(k, np.float32)
+        v = np.asarray(v, np.float32)
+        n = k.shape[0]
+        if not 1 <= n <= self.W:
+            raise ValueError("a write must carry 1 .. n_slots - n_global tokens")
+        if self.G and not self.globals_written:
+            raise ValueError("the global slots are written before the first window write")
+        slots = self.slots_for(n)
+        self._store(k, v, pos, slots)
+        self.wp = int((self.wp + n) % self.W)
         self.n_valid = int(min(self.n_valid + n, self.S))
+        return slots
+
+    def write_global(self, k, v, pos):
+        """The G global tokens of the session, once, into slots 0 .. G-1
+        (same arithmetic as a window write).  Returns their slots."""
+        k = np.asarray(k, np.float32)
+        v = np.asarray(v, np.float32)
+        if self.G == 0 or k.shape[0] != self.G:
+            raise ValueError("a global write carries exactly n_global tokens")
+        if self.globals_written or self.n_valid:
+            raise ValueError("the global slots are written once, before any window write")
+        slots = np.arange(self.G)
+        self._store(k, v, pos, slots)
+        self.globals_written = True
+        self.n_valid = self.G
         return slots
 
     # -- reset ---------------------------------------------------------------
     def reset_positions(self, d):
-        """Rotate every valid cached key by R(-d) on the temporal axis
-        (axis 0), in fp32, and re-quantise it with a fresh absmax scale."""
-        n = self.n_valid
-        if n == 0:
+        """Rotate every valid window key by R(-d) on the temporal axis
+        (axis 0), in fp32, and re-quantise it with a fresh absmax scale.
+        Global keys are not touched."""
+        lo, hi = self.G, self.n_valid
+        if hi <= lo:
             return
         c, s = rope.delta_cos_sin_f32(d, self.axis_dims[0], self.base)
-        k = quant.dequantize_rows(self.k_codes[:, :n], self.k_scale[:, :n])
+        k = quant.dequantize_rows(self.k_codes[:, lo:hi], self.k_scale[:, lo:hi])
         k = rope.rotate_temporal_f32(k, c, s, self.axis_dims[0])
         codes, scale = quant.quantize_rows(k)
-        self.k_codes[:, :n] = codes
-        self.k_scale[:, :n] = scale
+        self.k_codes[:, lo:hi] = codes
+        self.k_scale[:, lo:hi] = scale
 
     # -- attend --------------------------------------------------------------
     def quantized_queries(self, q, q_pos):

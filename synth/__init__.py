@@ -26,6 +26,12 @@ Workloads (the shapes the paper describes: 757 new tokens per write into a
 5. ``sweep``     H in {8,24,48} x D in {64,128} x S in {1447,2894,5788,11576},
                  N = round(S*757/5788), 3-axis (t,h,w) positions on a latent
                  grid with aspect 1088:704.
+6. ``windowed``  the paper's own layout: 1,246 global slots written once (at
+                 temporal positions -1246 .. -1), then a window ring of six
+                 757-token frames; ten steps of write(757)+attend(757) at
+                 (s mod 7)*757 + i, the window reset by 7*757 before step 7;
+                 1% of the channels x8.  ``windowed_tiny``: the same on
+                 H=2, D=64, 10 globals, three 16-token frames, 3-axis RoPE.
 """
 from __future__ import annotations
 
@@ -53,6 +59,7 @@ class Shape:
     pos_min: Tuple[int, ...]        # RoPE table coverage per axis: positions
     pos_count: Tuple[int, ...]      #   pos_min .. pos_min + pos_count - 1
     rope_base: float = 10000.0
+    n_global: int = 0               # global slots ahead of the window ring
 
     @property
     def n_axes(self):
@@ -64,6 +71,14 @@ class Write:
     k: torch.Tensor            # bf16 [N, H, D] (CPU)
     v: torch.Tensor
     pos: np.ndarray            # int32 [N, n_axes]
+    ring: int = 0
+
+
+@dataclass
+class WriteGlobal:
+    k: torch.Tensor            # bf16 [n_global, H, D] (CPU)
+    v: torch.Tensor
+    pos: np.ndarray            # int32 [n_global, n_axes]
     ring: int = 0
 
 
@@ -86,7 +101,7 @@ class Workload:
     name: str
     shape: Shape
     n_rings: int
-    ops: Iterator           # of Write / Reset / Attend
+    ops: Iterator           # of WriteGlobal / Write / Reset / Attend
     note: str = ""
 
 
@@ -292,3 +307,59 @@ def sweep(heads: int, head_dim: int, n_slots: int) -> Workload:
 
 def sweep_shapes():
     return [(h, d, s) for h in SWEEP_HEADS for d in SWEEP_DIMS for s in SWEEP_SLOTS]
+
+
+GLOBAL_SLOTS = 1246
+WINDOW_FRAMES = 6
+WINDOWED_PERIOD = 7
+WINDOWED_STEPS = 10
+
+
+def windowed(steps: int = WINDOWED_STEPS, period: int = WINDOWED_PERIOD) -> Workload:
+    """1,246 global tokens at temporal positions -1246 .. -1, written once;
+    then step s writes a 757-token frame at (s mod period)*757 + i and attends
+    757 queries at those positions; before steps period, 2*period, ... the
+    window is reset by period*757.  Seed 5; 1% of the channels x8."""
+    H, D, G, N = 24, 128, GLOBAL_SLOTS, NEW_TOKENS
+    S = G + WINDOW_FRAMES * N
+    dshift = period * N
+    shape = Shape(H, D, S, (D,), (-G,), (G + dshift,), n_global=G)
+
+    def ops():
+        g = rng(5)
+        ch = outlier_channels(g, H, D)
+        yield WriteGlobal(normal_bf16(g, (G, H, D), ch), normal_bf16(g, (G, H, D), ch), lin_pos(-G, G))
+        for s in range(steps):
+            if s > 0 and s % period == 0:
+                yield Reset(dshift)
+            pos = lin_pos((s % period) * N, N)
+            k = normal_bf16(g, (N, H, D), ch)
+            v = normal_bf16(g, (N, H, D), ch)
+            q = normal_bf16(g, (N, H, D), ch)
+            yield Write(k, v, pos)
+            yield Attend(q, pos, tag=f"s{s}")
+    return Workload("windowed", shape, 1, ops())
+
+
+def windowed_tiny(steps: int = 8, period: int = 4) -> Workload:
+    """H=2, D=64, 10 globals (t = -1, on a 4-wide grid), a window of three
+    16-token frames (t = s mod period, a 4x4 grid); reset by period before
+    step period; an attend after every write."""
+    H, D, G, N = 2, 64, 10, 16
+    S = G + 3 * N
+    shape = Shape(H, D, S, (16, 24, 24), (-1, 0, 0), (period + 1, 4, 4), n_global=G)
+
+    def grid(t, n):
+        i = np.arange(n)
+        return np.stack([np.full(n, t), i // 4, i % 4], axis=1).astype(np.int32)
+
+    def ops():
+        g = rng(6)
+        yield WriteGlobal(normal_bf16(g, (G, H, D)), normal_bf16(g, (G, H, D)), grid(-1, G))
+        for s in range(steps):
+            if s > 0 and s % period == 0:
+                yield Reset(period)
+            pos = grid(s % period, N)
+            yield Write(normal_bf16(g, (N, H, D)), normal_bf16(g, (N, H, D)), pos)
+            yield Attend(normal_bf16(g, (N, H, D)), pos, tag=f"t{s}")
+    return Workload("windowed_tiny", shape, 1, ops())

@@ -31,6 +31,7 @@ struct RingView {
   uint8_t* q_codes;               // query scratch: e4m3 [n_q][H][D]
   float* q_scale;                 // query scratch: fp32 [H][Q_pad]
   int32_t H, D, S, S_pad, n_axes, Q_pad;
+  int32_t G;                      // global slots 0 .. G-1; the window ring is slots G .. S-1
 };
 
 // ---------------------------------------------------------------- numerics

@@ -28,6 +28,9 @@ struct kvring {
   AttnMaps maps;
   CUtensorMap q_map;  // e4m3 query scratch, [max_queries][H][D]
   int device;
+  // call order, tracked on the host (the calls are enqueued in host order)
+  bool globals_written;
+  bool window_written;
 };
 
 namespace {
@@ -64,6 +67,7 @@ bool check_config(const kvring_config* c) {
   if (!(c->rope_base > 1.0) || !std::isfinite(c->rope_base)) return false;
   if (c->out_dtype != KVRING_OUT_BF16 && c->out_dtype != KVRING_OUT_F32) return false;
   if (c->max_queries < 1 || c->max_queries > (1 << 20)) return false;
+  if (c->n_global < 0 || c->n_global >= c->n_slots) return false;
   return true;
 }
 
@@ -244,6 +248,7 @@ int kvring_create(const kvring_config* cfg, void* workspace, size_t workspace_by
   rv.S = cfg->n_slots;
   rv.S_pad = L.s_pad;
   rv.n_axes = cfg->n_axes;
+  rv.G = cfg->n_global;
 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   // state, codes and scales (and the query scratch) start at zero: an empty ring
@@ -285,11 +290,26 @@ int kvring_create(const kvring_config* cfg, void* workspace, size_t workspace_by
 int kvring_write(kvring* r, const void* k, const void* v, const int32_t* pos, int32_t n_new,
                  kvring_stream stream) {
   if (!r || !k || !v || !pos) return KVRING_ERR_INVALID_ARG;
-  if (n_new < 1 || n_new > r->rv.S) return KVRING_ERR_INVALID_ARG;
+  if (n_new < 1 || n_new > r->rv.S - r->rv.G) return KVRING_ERR_INVALID_ARG;
   if (!aligned(k, 16) || !aligned(v, 16) || !aligned(pos, 4)) return KVRING_ERR_MISALIGNED;
+  if (r->rv.G > 0 && !r->globals_written) return KVRING_ERR_SEQUENCE;
   const cudaError_t e =
-      launch_ring_kv_write(r->rv, k, v, pos, n_new, reinterpret_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? KVRING_OK : cuda_fail(e);
+      launch_ring_kv_write(r->rv, k, v, pos, n_new, false, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  r->window_written = true;
+  return KVRING_OK;
+}
+
+int kvring_write_global(kvring* r, const void* k, const void* v, const int32_t* pos, int32_t n,
+                        kvring_stream stream) {
+  if (!r || !k || !v || !pos) return KVRING_ERR_INVALID_ARG;
+  if (r->rv.G == 0 || n != r->rv.G) return KVRING_ERR_INVALID_ARG;
+  if (!aligned(k, 16) || !aligned(v, 16) || !aligned(pos, 4)) return KVRING_ERR_MISALIGNED;
+  if (r->globals_written || r->window_written) return KVRING_ERR_SEQUENCE;
+  const cudaError_t e = launch_ring_kv_write(r->rv, k, v, pos, n, true, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  r->globals_written = true;
+  return KVRING_OK;
 }
 
 int kvring_reset_positions(kvring* r, int32_t d, kvring_stream stream) {
@@ -361,6 +381,8 @@ const char* kvring_status_string(int s) {
     case KVRING_ERR_NO_DEVICE: return "no sm_100-family device is current";
     case KVRING_ERR_SCRATCH_LIMIT:
       return "request larger than the static scratch of kvring_attend_noalloc (KVRING_NOALLOC_SCRATCH_BYTES)";
+    case KVRING_ERR_SEQUENCE:
+      return "call out of order: the global slots are written once, before the first window write";
     default: return "unknown status";
   }
 }

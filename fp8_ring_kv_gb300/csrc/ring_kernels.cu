@@ -4,6 +4,10 @@
 // position), §4.2 (RoPE at write; delta rotation at reset), §4.3 (FP8 at
 // write), Appendix G (cache update and position reset).
 //
+// Slots 0 .. G-1 hold the session's global tokens (written once, never
+// rotated); the window ring is slots G .. S-1, W = S - G of them (G = 0: the
+// whole cache is the ring).
+//
 // Both kernels stream rows of one (token or slot, head): a row of D channels
 // is handled by L = D/16 consecutive lanes, each owning 16 channels (32 bytes
 // of bf16 in, 16 bytes of e4m3 out), so every global access is a full 16-byte
@@ -37,10 +41,15 @@ __device__ __forceinline__ unsigned row_group_mask() {
 // the block; as soon as it has, the block counts itself in, and the last
 // block to do so advances the ring state (every block has read the position
 // by then).  No barrier waits for the stores.
+//
+// Window write: token i goes to slot G + (wp + i) mod W; then wp <- (wp + N)
+// mod W and n_valid <- min(n_valid + N, S).  Global write (``glob``, the G
+// global tokens, once): token i goes to slot i; then n_valid <- N.
 template <int L>
 __global__ void __launch_bounds__(512, 2) ring_kv_write_kernel(RingView rv, const uint4* __restrict__ k,
                                                                const uint4* __restrict__ v,
-                                                               const int32_t* __restrict__ pos, int n_new, int T) {
+                                                               const int32_t* __restrict__ pos, int n_new, int T,
+                                                               bool glob) {
   constexpr int D = L * 16;
   __shared__ int wp_s;
   const int H = rv.H;
@@ -74,17 +83,22 @@ __global__ void __launch_bounds__(512, 2) ring_kv_write_kernel(RingView rv, cons
   if (threadIdx.x == 0) wp_s = rv.state[ST_WP];
   __syncthreads();
   const int wp = wp_s;
+  const int W = rv.S - rv.G;
   if (threadIdx.x == 0) {
     const int done = atomicAdd(&rv.state[ST_DONE], 1);
     if (done == (int)gridDim.x - 1) {
-      rv.state[ST_WP] = (int)(((long long)wp + n_new) % rv.S);
-      rv.state[ST_NVALID] = min(rv.state[ST_NVALID] + n_new, rv.S);
+      if (glob) {
+        rv.state[ST_NVALID] = n_new;
+      } else {
+        rv.state[ST_WP] = (int)(((long long)wp + n_new) % W);
+        rv.state[ST_NVALID] = min(rv.state[ST_NVALID] + n_new, rv.S);
+      }
       rv.state[ST_DONE] = 0;
     }
   }
   if (!live) return;
 
-  const int slot = (int)(((long long)wp + tok) % rv.S);
+  const int slot = glob ? tok : rv.G + (int)(((long long)wp + tok) % W);
   const size_t row = (size_t)h * rv.S + slot;
   const unsigned gm = row_group_mask<L>();
   {
@@ -162,7 +176,8 @@ __global__ void __launch_bounds__(512, 2) q_prep_kernel(RingView rv, const uint4
 }
 
 // ---------------------------------------------------------------- delta_rerotate
-// In place over the key rows (head, slot) with slot < n_valid: dequantise
+// In place over the window's key rows (head, slot), G <= slot < n_valid
+// (the global keys keep their positions): dequantise
 // (code * scale, fp32), rotate the temporal pairs by the host-computed
 // (cos, sin) of -d * omega_j, re-quantise with a fresh absmax scale.  A row
 // is L lanes of 16 codes; the grid is sized to stay resident and each thread
@@ -178,9 +193,10 @@ __global__ void __launch_bounds__(256) delta_rerotate_kernel(RingView rv, DeltaT
   pdl_wait();
   pdl_trigger();
   __syncthreads();
-  const int n_valid = rv.state[ST_NVALID];
-  if (n_valid <= 0) return;
-  const int chunks = rv.H * n_valid * L;          // <= 128 heads x 2^20 slots x 8
+  // rows are walked as (h, s) over the n_win valid window slots, s = slot - G
+  const int n_win = rv.state[ST_NVALID] - rv.G;
+  if (n_win <= 0) return;
+  const int chunks = rv.H * n_win * L;            // <= 128 heads x 2^20 slots x 8
   const int stride = gridDim.x * blockDim.x;      // a multiple of 32: rows never split
   const int lane = threadIdx.x % L;
   // pairs past the temporal axis are left as they are (not rotated by the
@@ -191,15 +207,15 @@ __global__ void __launch_bounds__(256) delta_rerotate_kernel(RingView rv, DeltaT
   // the thread's row (head h, slot) advances by a fixed number of rows per
   // step: kept as (h, slot) and carried, instead of two divisions per row
   const int row_step = stride / L;
-  const int step_h = row_step / n_valid;
-  const int step_slot = row_step - step_h * n_valid;
+  const int step_h = row_step / n_win;
+  const int step_slot = row_step - step_h * n_win;
   int c = blockIdx.x * blockDim.x + threadIdx.x;
   if (c >= chunks) return;   // whole rows
-  int h = (c / L) / n_valid;
-  int slot = c / L - h * n_valid;
+  int h = (c / L) / n_win;
+  int slot = c / L - h * n_win;
   auto locate = [&](int hh, int ss, uint8_t*& p, float*& sp) {
-    p = rv.k_codes + ((size_t)hh * rv.S + ss) * D + lane * 16;
-    sp = rv.k_scale + (size_t)hh * rv.S_pad + ss;
+    p = rv.k_codes + ((size_t)hh * rv.S + rv.G + ss) * D + lane * 16;
+    sp = rv.k_scale + (size_t)hh * rv.S_pad + rv.G + ss;
   };
   uint8_t* p;
   float* sp;
@@ -214,8 +230,8 @@ __global__ void __launch_bounds__(256) delta_rerotate_kernel(RingView rv, DeltaT
     uint4 code_n = code;
     float scale_n = scale;
     int hn = h + step_h, sn = slot + step_slot;
-    if (sn >= n_valid) {
-      sn -= n_valid;
+    if (sn >= n_win) {
+      sn -= n_win;
       ++hn;
     }
     if (more) {
@@ -281,20 +297,20 @@ __global__ void __launch_bounds__(256) debug_quantize_kernel(const float* __rest
 // ---------------------------------------------------------------- launchers
 template <int L>
 static cudaError_t launch_write_t(const RingView& rv, const void* k, const void* v, const int32_t* pos, int n_new,
-                                  cudaStream_t st) {
+                                  bool glob, cudaStream_t st) {
   const int per_tok = rv.H * L;
   int T = 192 / per_tok;
   if (T < 1) T = 1;
   const int threads = per_tok * T;
   const int blocks = (n_new + T - 1) / T;
   return launch_pdl(ring_kv_write_kernel<L>, dim3(blocks), dim3(threads), 0, st, rv, static_cast<const uint4*>(k),
-                    static_cast<const uint4*>(v), pos, n_new, T);
+                    static_cast<const uint4*>(v), pos, n_new, T, glob);
 }
 
 cudaError_t launch_ring_kv_write(const RingView& rv, const void* k, const void* v, const int32_t* pos, int n_new,
-                                 cudaStream_t st) {
-  if (rv.D == 64) return launch_write_t<4>(rv, k, v, pos, n_new, st);
-  return launch_write_t<8>(rv, k, v, pos, n_new, st);
+                                 bool glob, cudaStream_t st) {
+  if (rv.D == 64) return launch_write_t<4>(rv, k, v, pos, n_new, glob, st);
+  return launch_write_t<8>(rv, k, v, pos, n_new, glob, st);
 }
 
 cudaError_t launch_q_prep(const RingView& rv, const void* q, const int32_t* q_pos, int n_q, cudaStream_t st) {

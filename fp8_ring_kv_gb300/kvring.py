@@ -21,6 +21,7 @@ KVRING_ERR_CUDA = -4
 KVRING_ERR_WORKSPACE = -5
 KVRING_ERR_NO_DEVICE = -6
 KVRING_ERR_SCRATCH_LIMIT = -7
+KVRING_ERR_SEQUENCE = -8
 KVRING_NOALLOC_SCRATCH_BYTES = 8 << 20
 
 KVRING_DEVERR_POS_RANGE = 1
@@ -31,7 +32,7 @@ KVRING_OUT_BF16 = 0
 KVRING_OUT_F32 = 1
 
 EXPORTS = (
-    "kvring_workspace_bytes", "kvring_create", "kvring_write", "kvring_reset_positions",
+    "kvring_workspace_bytes", "kvring_create", "kvring_write", "kvring_write_global", "kvring_reset_positions",
     "kvring_attend", "kvring_destroy", "kvring_status_string", "kvring_last_cuda_error",
     "kvring_layout", "kvring_debug_state", "kvring_debug_quantize",
 )
@@ -49,6 +50,7 @@ class kvring_config(ctypes.Structure):
         ("rope_base", ctypes.c_double),
         ("out_dtype", ctypes.c_int32),
         ("max_queries", ctypes.c_int32),
+        ("n_global", ctypes.c_int32),
     ]
 
 
@@ -73,6 +75,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "kvring_workspace_bytes": (sz, [cfgp]),
         "kvring_create": (ctypes.c_int, [cfgp, vp, sz, vp, ctypes.POINTER(vp)]),
         "kvring_write": (ctypes.c_int, [vp, vp, vp, vp, i32, vp]),
+        "kvring_write_global": (ctypes.c_int, [vp, vp, vp, vp, i32, vp]),
         "kvring_reset_positions": (ctypes.c_int, [vp, i32, vp]),
         "kvring_attend": (ctypes.c_int, [vp, vp, vp, i32, vp, vp]),
         "kvring_attend_noalloc": (ctypes.c_int, [vp, vp, vp, i32, vp, vp]),
@@ -112,7 +115,7 @@ def _ptr(t) -> ctypes.c_void_p:
 
 
 def make_config(heads, head_dim, n_slots, axis_dims, pos_min, pos_count, rope_base=10000.0,
-                out_dtype=KVRING_OUT_F32, max_queries=None) -> kvring_config:
+                out_dtype=KVRING_OUT_F32, max_queries=None, n_global=0) -> kvring_config:
     """max_queries defaults to n_slots (a call attends at most one ring's worth of queries)."""
     c = kvring_config()
     c.heads, c.head_dim, c.n_slots = int(heads), int(head_dim), int(n_slots)
@@ -124,6 +127,7 @@ def make_config(heads, head_dim, n_slots, axis_dims, pos_min, pos_count, rope_ba
     c.rope_base = float(rope_base)
     c.out_dtype = int(out_dtype)
     c.max_queries = int(n_slots if max_queries is None else max_queries)
+    c.n_global = int(n_global)
     return c
 
 
@@ -141,6 +145,11 @@ def kvring_create(cfg: kvring_config, workspace: torch.Tensor, stream=None) -> c
 
 def kvring_write(handle, k, v, pos, n_new: int, stream=None) -> None:
     check(load().kvring_write(handle, _ptr(k), _ptr(v), _ptr(pos), int(n_new), _stream(stream)), "kvring_write")
+
+
+def kvring_write_global(handle, k, v, pos, n: int, stream=None) -> None:
+    check(load().kvring_write_global(handle, _ptr(k), _ptr(v), _ptr(pos), int(n), _stream(stream)),
+          "kvring_write_global")
 
 
 def kvring_reset_positions(handle, d: int, stream=None) -> None:
@@ -176,13 +185,14 @@ class KVRing:
     the current (or given) stream and return at once."""
 
     def __init__(self, heads, head_dim, n_slots, axis_dims, pos_min, pos_count, rope_base=10000.0,
-                 out_dtype=KVRING_OUT_F32, device="cuda", stream=None, max_queries=None):
+                 out_dtype=KVRING_OUT_F32, device="cuda", stream=None, max_queries=None, n_global=0):
         self.cfg = make_config(heads, head_dim, n_slots, axis_dims, pos_min, pos_count, rope_base, out_dtype,
-                               max_queries)
+                               max_queries, n_global)
         nbytes = kvring_workspace_bytes(self.cfg)
         if nbytes == 0:
             raise KVRingError("invalid kvring configuration")
         self.heads, self.head_dim, self.n_slots = int(heads), int(head_dim), int(n_slots)
+        self.n_global = int(n_global)
         self.n_axes = len(axis_dims)
         self.out_dtype = torch.float32 if out_dtype == KVRING_OUT_F32 else torch.bfloat16
         self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=device)
@@ -205,10 +215,13 @@ class KVRing:
     @classmethod
     def from_shape(cls, shape, out_dtype=KVRING_OUT_F32, device="cuda", stream=None, max_queries=None):
         return cls(shape.heads, shape.head_dim, shape.n_slots, shape.axis_dims, shape.pos_min, shape.pos_count,
-                   shape.rope_base, out_dtype, device, stream, max_queries)
+                   shape.rope_base, out_dtype, device, stream, max_queries, getattr(shape, "n_global", 0))
 
     def write(self, k, v, pos, stream=None):
         kvring_write(self.handle, k, v, pos, k.shape[0], stream)
+
+    def write_global(self, k, v, pos, stream=None):
+        kvring_write_global(self.handle, k, v, pos, k.shape[0], stream)
 
     def reset_positions(self, d, stream=None):
         kvring_reset_positions(self.handle, d, stream)

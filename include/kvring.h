@@ -4,6 +4,8 @@
  *
  * Source: "Runway Characters: Serving a 57B Video Diffusion Transformer for
  * Real-Time Conversation" (arXiv:2611.05642):
+ *   Introduction ("The model") and App. G  each cache holds global slots,
+ *         written once per session, ahead of a window ring of latent frames;
  *   §4.1  a ring cache with a device-side write position;
  *   §4.2  RoPE applied once at write, and a delta rotation of the cached keys
  *         when positions reset;
@@ -57,7 +59,8 @@ enum {
   KVRING_ERR_UNSUPPORTED = -3,  /* shape outside the kernels' set (see kvring_config) */
   KVRING_ERR_CUDA = -4,         /* a CUDA runtime/driver call failed; kvring_last_cuda_error says which */
   KVRING_ERR_WORKSPACE = -5,    /* workspace too small */
-  KVRING_ERR_NO_DEVICE = -6     /* no sm_100-family GPU is current */
+  KVRING_ERR_NO_DEVICE = -6,    /* no sm_100-family GPU is current */
+  KVRING_ERR_SEQUENCE = -8      /* call out of order (global slots: once, before any window write) */
 };
 
 /* bits of the device-side error word */
@@ -91,6 +94,12 @@ enum { KVRING_OUT_BF16 = 0, KVRING_OUT_F32 = 1 };
  *              (max_queries * H * D bytes + their fp32 scales) as per-call
  *              scratch, so two kvring_attend calls on one ring must not run
  *              at the same time (in stream order they may follow each other)
+ *   n_global   0 .. n_slots-1 global slots (Introduction, "The model"; App. G:
+ *              1,246 in the paper's caches).  Slots 0 .. n_global-1 hold the
+ *              session's global tokens, written once by kvring_write_global
+ *              and never rotated; the window ring is slots n_global ..
+ *              n_slots-1 (W = n_slots - n_global of them).  0: the whole
+ *              cache is the window ring.
  */
 typedef struct {
   int32_t heads;
@@ -103,6 +112,7 @@ typedef struct {
   double rope_base;
   int32_t out_dtype;
   int32_t max_queries;
+  int32_t n_global;
 } kvring_config;
 
 /* Bytes of device workspace kvring_create needs for this configuration
@@ -126,24 +136,43 @@ int kvring_create(const kvring_config* cfg, void* workspace, size_t workspace_by
  * at write), §4.1 (ring slot at the device-side write position).
  *   k, v   device bf16 [n_new][H][D], 16-byte aligned; not modified
  *   pos    device int32 [n_new][n_axes], 4-byte aligned
- *   n_new  1 .. n_slots
+ *   n_new  1 .. W (= n_slots - n_global)
  * For token i and head h: K is rotated by RoPE at pos[i] in fp32, V is not;
  * each (token, head) row of K and of V gets one fp32 scale amax/448 and e4m3
  * codes round-to-nearest-even(x * (448/amax)) saturated to +-448; they go to
- * slot (wp + i) mod S, where wp is the device-side write position.  Then, on
- * the device, wp <- (wp + n_new) mod S and n_valid <- min(n_valid + n_new, S).
+ * slot n_global + (wp + i) mod W, where wp is the device-side write position.
+ * Then, on the device, wp <- (wp + n_new) mod W and
+ * n_valid <- min(n_valid + n_new, S).  With n_global > 0 the global slots
+ * must have been written first (else KVRING_ERR_SEQUENCE).
  */
 int kvring_write(kvring* r, const void* k, const void* v, const int32_t* pos, int32_t n_new,
                  kvring_stream stream);
 
 /*
+ * Write the session's n_global global tokens (ring_kv_write), once, before
+ * the first kvring_write.  Introduction ("The model") and App. G: the global
+ * slots are written once per session; a position reset does not move them.
+ *   k, v, pos  as kvring_write, with n rows
+ *   n          exactly n_global (else KVRING_ERR_INVALID_ARG, also when the
+ *              ring has no global slots)
+ * Same arithmetic as kvring_write; token i goes to slot i, and then, on the
+ * device, n_valid <- n_global (wp stays 0).  A second call, or one after a
+ * kvring_write, returns KVRING_ERR_SEQUENCE before anything is enqueued (the
+ * order is checked on the host, in the order the calls are made).
+ */
+int kvring_write_global(kvring* r, const void* k, const void* v, const int32_t* pos, int32_t n,
+                        kvring_stream stream);
+
+/*
  * Position reset by d (delta_rerotate).  Paper §4.2 and App. G: every cached
  * key moves from temporal position p to p - d; with RoPE angles affine in the
  * position, that is one rotation R(-d * omega_{0,j}) of each temporal-axis
- * pair.  Every valid key row is dequantised (code * scale, fp32), its
- * temporal pairs are rotated in fp32 by the fp32-rounded cos/sin of
- * -d * omega_{0,j} (formed in fp64 on the host), and the row is re-quantised
- * with a fresh absmax scale, in place.  Values are not touched.  ``d`` is a
+ * pair.  Every valid window key row (slots n_global .. n_valid-1: the global
+ * keys' positions do not depend on the window) is dequantised (code * scale,
+ * fp32), its temporal pairs are rotated in fp32 by the fp32-rounded cos/sin
+ * of -d * omega_{0,j} (formed in fp64 on the host), and the row is
+ * re-quantised with a fresh absmax scale, in place.  Values and global keys
+ * are not touched.  ``d`` is a
  * host value and is baked into a captured graph.  Callers pass positions
  * shifted by -d to later calls; the library keeps no position counter.
  */

@@ -78,18 +78,20 @@ def replay(wl: synth.Workload, *, cache_every=1, attend_filter=None, oracle_ring
     sh = wl.shape
     rings = [gpu_ring(sh, out_f32) for _ in range(wl.n_rings)]
     follow = set(range(wl.n_rings)) if oracle_rings is None else set(oracle_rings)
-    refs = {r: OracleRing(sh.heads, sh.head_dim, sh.n_slots, sh.axis_dims, sh.rope_base) for r in follow}
+    refs = {r: OracleRing(sh.heads, sh.head_dim, sh.n_slots, sh.axis_dims, sh.rope_base, n_global=sh.n_global)
+            for r in follow}
     rep = Report()
     n_cache = 0
     dev = torch.device("cuda")
     for op in wl.ops:
         g = rings[op.ring]
         o = refs.get(op.ring)
-        if isinstance(op, synth.Write):
-            g.write(op.k.to(dev), op.v.to(dev), torch.from_numpy(op.pos).to(dev))
+        if isinstance(op, (synth.Write, synth.WriteGlobal)):
+            glob = isinstance(op, synth.WriteGlobal)
+            (g.write_global if glob else g.write)(op.k.to(dev), op.v.to(dev), torch.from_numpy(op.pos).to(dev))
             rep.writes += 1
             if o is not None:
-                o.write(synth.to_f32(op.k), synth.to_f32(op.v), op.pos)
+                (o.write_global if glob else o.write)(synth.to_f32(op.k), synth.to_f32(op.v), op.pos)
                 wp, nv, err = g.debug_state()
                 assert (wp, nv, err) == (o.wp, o.n_valid, 0), f"state {(wp, nv, err)} vs {(o.wp, o.n_valid)}"
                 n_cache += 1

@@ -70,12 +70,16 @@ def test_workspace_bytes_valid_configuration(lib):
     assert K.kvring_workspace_bytes(paper_config(n_slots=S + 1000)) > n
     assert K.kvring_workspace_bytes(paper_config(max_queries=2 * S)) > n
     assert K.kvring_workspace_bytes(paper_config(max_queries=1)) < n
+    # global slots are part of the n_slots, not extra
+    assert K.kvring_workspace_bytes(paper_config(n_global=1246)) == n
+    assert K.kvring_workspace_bytes(paper_config(n_global=5787)) == n
 
 
 @pytest.mark.parametrize("field,value", [
     ("head_dim", 96), ("head_dim", 256), ("heads", 0), ("n_slots", 0), ("n_slots", (1 << 20) + 1),
     ("n_axes", 0), ("n_axes", 4), ("rope_base", 1.0), ("rope_base", math.nan), ("rope_base", math.inf),
     ("out_dtype", 7), ("max_queries", 0), ("max_queries", (1 << 20) + 1),
+    ("n_global", -1), ("n_global", 5788), ("n_global", 6000),
 ])
 def test_workspace_bytes_rejects_invalid(lib, field, value):
     assert K.kvring_workspace_bytes(paper_config(**{field: value})) == 0
@@ -95,7 +99,8 @@ def test_workspace_bytes_rejects_bad_axes(lib):
 
 def test_status_strings(lib):
     codes = [K.KVRING_OK, K.KVRING_ERR_INVALID_ARG, K.KVRING_ERR_MISALIGNED, K.KVRING_ERR_UNSUPPORTED,
-             K.KVRING_ERR_CUDA, K.KVRING_ERR_WORKSPACE, K.KVRING_ERR_NO_DEVICE, K.KVRING_ERR_SCRATCH_LIMIT]
+             K.KVRING_ERR_CUDA, K.KVRING_ERR_WORKSPACE, K.KVRING_ERR_NO_DEVICE, K.KVRING_ERR_SCRATCH_LIMIT,
+             K.KVRING_ERR_SEQUENCE]
     texts = [lib.kvring_status_string(c).decode() for c in codes]
     assert len(set(texts)) == len(texts) and all(texts)
     assert lib.kvring_status_string(12345).decode() == "unknown status"
@@ -126,6 +131,7 @@ def test_create_rejects_before_any_cuda_call(lib):
 def test_calls_on_null_handle(lib):
     p = _vp(1 << 20)
     assert lib.kvring_write(None, p, p, p, 1, None) == K.KVRING_ERR_INVALID_ARG
+    assert lib.kvring_write_global(None, p, p, p, 1, None) == K.KVRING_ERR_INVALID_ARG
     assert lib.kvring_reset_positions(None, 5, None) == K.KVRING_ERR_INVALID_ARG
     assert lib.kvring_attend(None, p, p, 1, p, None) == K.KVRING_ERR_INVALID_ARG
     assert lib.kvring_attend_noalloc(None, p, p, 1, p, None) == K.KVRING_ERR_INVALID_ARG

@@ -139,3 +139,56 @@ def test_write_of_a_whole_ring_then_wrapping_writes():
     out = ring.attend(q.to(dev), torch.from_numpy(qpos).to(dev)).cpu().numpy()
     compare_attention(out, o.attend(synth.to_f32(q), qpos), "attend after wraps")
     ring.close()
+
+
+def test_global_slot_call_order_is_checked_on_the_host():
+    """kvring_write_global: exactly n_global tokens, once, before any window
+    write; window writes carry at most n_slots - n_global tokens.  Rejected
+    calls enqueue nothing."""
+    K, lib = _lib()
+    sh = synth.Shape(2, 64, 40, (64,), (0,), (256,), n_global=8)
+    ring = _ring(sh)
+    dev = torch.device("cuda")
+    k = torch.zeros((40, sh.heads, sh.head_dim), dtype=torch.bfloat16, device=dev)
+    pos = torch.zeros((40, 1), dtype=torch.int32, device=dev)
+    h = ring.handle
+    p = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
+    assert lib.kvring_write(h, p(k), p(k), p(pos), 4, None) == K.KVRING_ERR_SEQUENCE
+    assert lib.kvring_write_global(h, p(k), p(k), p(pos), 7, None) == K.KVRING_ERR_INVALID_ARG
+    assert lib.kvring_write_global(h, p(k), p(k), p(pos), 9, None) == K.KVRING_ERR_INVALID_ARG
+    torch.cuda.synchronize()
+    assert ring.debug_state() == (0, 0, 0)
+    assert lib.kvring_write_global(h, p(k), p(k), p(pos), 8, None) == K.KVRING_OK
+    assert lib.kvring_write_global(h, p(k), p(k), p(pos), 8, None) == K.KVRING_ERR_SEQUENCE
+    assert lib.kvring_write(h, p(k), p(k), p(pos), 33, None) == K.KVRING_ERR_INVALID_ARG
+    torch.cuda.synchronize()
+    assert ring.debug_state() == (0, 8, 0)
+    assert lib.kvring_write(h, p(k), p(k), p(pos), 32, None) == K.KVRING_OK
+    torch.cuda.synchronize()
+    assert ring.debug_state() == (0, 40, 0)
+    ring.close()
+    plain = _ring(_tiny_shape())
+    assert lib.kvring_write_global(plain.handle, p(k), p(k), p(pos), 1, None) == K.KVRING_ERR_INVALID_ARG
+    plain.close()
+
+
+def test_reset_before_any_window_write_leaves_the_globals():
+    """A reset with only the globals written rotates nothing."""
+    sh = synth.Shape(2, 64, 40, (16, 24, 24), (-8, 0, 0), (16, 4, 4), n_global=8)
+    ring = _ring(sh)
+    o = OracleRing(sh.heads, sh.head_dim, sh.n_slots, sh.axis_dims, sh.rope_base, n_global=8)
+    g = synth.rng(79)
+    k = synth.normal_bf16(g, (8, sh.heads, sh.head_dim))
+    v = synth.normal_bf16(g, (8, sh.heads, sh.head_dim))
+    pos = np.stack([np.full(8, -1), np.arange(8) // 4, np.arange(8) % 4], 1).astype(np.int32)
+    ring.write_global(k.cuda(), v.cuda(), torch.from_numpy(pos).cuda())
+    o.write_global(synth.to_f32(k), synth.to_f32(v), pos)
+    ring.reset_positions(5)
+    o.reset_positions(5)
+    assert ring.debug_state() == (0, 8, 0)
+    compare_cache(ring, o, "globals after a reset")
+    q = synth.normal_bf16(g, (5, sh.heads, sh.head_dim))
+    qpos = np.stack([np.arange(5), np.zeros(5), np.zeros(5)], 1).astype(np.int32)
+    out = ring.attend(q.cuda(), torch.from_numpy(qpos).cuda()).cpu().numpy()
+    compare_attention(out, o.attend(synth.to_f32(q), qpos), "attend over the globals alone")
+    ring.close()

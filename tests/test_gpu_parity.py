@@ -59,3 +59,28 @@ def test_chunk_workload_sampled_rings():
 def test_sweep(heads, head_dim, n_slots):
     rep = replay(synth.sweep(heads, head_dim, n_slots), cache_every=3)
     assert rep.attend_checked == 1
+
+
+def test_global_slots_tiny_3axis():
+    """Global slots written once, a 3-frame window ring that wraps twice, a
+    reset that must leave the globals alone; everything compared after every
+    call."""
+    rep = replay(synth.windowed_tiny())
+    assert rep.writes == 9 and rep.resets == 1 and rep.attend_checked == 8
+    print("windowed_tiny", rep.attend_stats)
+
+
+def test_global_slots_tiny_bf16_output():
+    rep = replay(synth.windowed_tiny(), out_f32=False)
+    assert rep.attend_checked == 8
+
+
+def test_global_slots_at_paper_layout():
+    """1,246 globals + six 757-token frames (5,788 slots), ten steps with a
+    reset before step 7: cache bit for bit after every call; attention
+    checked when the window is first full, after the first wrap, right after
+    the reset and at the end."""
+    keep = {"s0", "s5", "s6", "s7", "s9"}
+    rep = replay(synth.windowed(), attend_filter=lambda t: t in keep)
+    assert rep.writes == 11 and rep.resets == 1 and rep.attend_checked == len(keep)
+    print("windowed", rep.attend_stats, f"{rep.seconds:.1f}s")

@@ -47,7 +47,7 @@ RESET_D = synth.RESET_PERIOD * N
 METRIC = "fp8_ring_attn calls/s + write/rerotate HBM GB/s at 5788 slots, 757 new"
 WORKLOAD = "single attention call at the paper's shape: 24 heads x 128, 5788-slot FP8 ring, 757 new tokens"
 
-# algorithmic work per launch
+# algorithmic work per launch: bytes each kernel must move, flops of the two contractions
 WRITE_BYTES = N * H * (6 * D + 8) + 4 * N * 1          # bf16 K,V in; e4m3 K,V + 2 fp32 scales out; positions
 REROT_BYTES = S * H * (2 * D + 8)                      # K codes + K scale, read and written
 ATTN_FLOPS = 4 * N * S * D * H                         # QK^T and PV
@@ -55,9 +55,9 @@ ATTN_FLOPS = 4 * N * S * D * H                         # QK^T and PV
 # (query RoPE + e4m3, then fp8_ring_attn)
 KERNELS_PER_STEP = 4
 # DRAM bytes (read + write) of one fp8_ring_attn launch at this workload, from
-# one ncu capture (profiles/fp8_ring_attn_single_call.md); set to None when
-# the kernel changes until it is captured again
-ATTN_DRAM_BYTES = 39_161_344 + 1_536
+# one ncu capture of the kernel as it stands; None while the kernel has
+# changed since the last capture (the row sums now come from the tensor core)
+ATTN_DRAM_BYTES = None
 
 
 # ---------------------------------------------------------------- distributed helpers

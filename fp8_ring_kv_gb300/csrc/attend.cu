@@ -12,30 +12,41 @@
 //
 //   S_j  = Qcodes . Kcodes_j^T            tcgen05 kind::f8f6f4, fp32 in TMEM
 //   t    = S_j * s_k (per column);  logit*log2(e) = t * s_q * log2(e)/sqrt(D)
-//   online softmax in base 2: e = exp2(t*r - m + c), l += e, with a running
-//   row maximum m that is only raised (and O rescaled) when a tile's maximum
+//   online softmax in base 2: e = exp2(t*r - m + c), with a running row
+//   maximum m that is only raised (and O, L rescaled) when a tile's maximum
 //   exceeds it by more than 2^14, so e <= 2^14 * 2^c
-//   P_j  = e * s_v (per column) rounded to fp16, in TMEM
+//   P_j  = e * w (per column, w = max(s_v, floor)) rounded to fp16, in TMEM
 //   O   += P_j . Vcodes_j                  tcgen05 kind::f16 (A = P from TMEM)
-//   out  = O / l
+//   L   += P_j . [u_hi | u_lo]_j           the same, N = 16: u = 2^-c / w
+//   out  = O / (L * 2^c)
 // The e4m3 V codes are widened to fp16 in shared memory (exact) because the
 // fp16 MMA takes both operands in fp16; P in fp16 keeps the weighted sum of V
 // within the accuracy that e4m3 weights would lose.  2^c is a per-head power of
-// two (cancelling between O and l) that keeps P within fp16 range.
+// two (cancelling between O and L) that keeps P within fp16 range.
 //
-// Pipeline.  S and P have two TMEM buffers each (S: 2 x 128 columns, P: 2 x
-// 64, O: 128).  The MMA sequence is QK_0, QK_1, QK_2, PV_0, QK_3, PV_1, ...:
-// while the softmax works on tile j the tensor cores run QK_{j+1} and
-// PV_{j-1}, and each MMA waits only for the softmax of the tile it consumes or
-// frees.  TMEM lane quarter q can only be read by the warps of SM
+// The row sums L are taken from the same fp16 P as the weighted sum of V (u
+// split into two fp16 parts, u_hi + u_lo * 2^-11, good to about 2^-22), so the
+// rounding of each P cancels between O and L: a row dominated by one slot
+// returns that slot's value, not the value times the fp16 rounding of its
+// weight (up to 2^-11 of |v|).  The per-head floor, 2^-15 * max(max s_v,
+// 2^-c), keeps a zero or near-zero V row's weight in L; it changes that row's
+// own (near-zero) values by at most 448 * floor.
+//
+// Pipeline.  S has two TMEM buffers (2 x 128 columns), P one (64), then L (16
+// of 32 columns) and O (D).  The MMA sequence is QK_0, QK_1, QK_2, PV_0, QK_3,
+// PV_1, ...: while the softmax works on tile j the tensor cores run QK_{j+1}
+// and PV_{j-1} (with its row sums), and each MMA waits only for the softmax of
+// the tile it consumes or frees; the softmax of tile j stores its P once
+// PV_{j-1} has read the previous one.  TMEM lane quarter q can only be read by the warps of SM
 // sub-partition q, so the softmax of rows 32q .. 32q+31 runs on one
 // sub-partition and its per-tile cost sets the pace.
 //
 // Warp roles (448 threads):
 //   warps 0-7   softmax: warp w serves the 16-lane half w/4 of TMEM lane
 //               quarter w%4; finally the output, half of the columns each
-//   warps 8-11  the per-head fp16 range factor, then the per-tile widening
-//               of V to fp16 (one warp per SM sub-partition)
+//   warps 8-11  the per-head fp16 range factor and scale floor, then per
+//               tile the widening of V to fp16 and the u columns (one warp
+//               per SM sub-partition)
 //   warp 12     TMA producer (the e4m3 query tile, then K, V codes into 4
 //               stages and their scales into 8)
 //   warp 13     TMEM allocation and MMA issue
@@ -62,13 +73,22 @@ constexpr int WARP_TMA = SOFT_WARPS + CONV_WARPS;
 constexpr int WARP_MMA = WARP_TMA + 1;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TM_S = 0;      // S buffer b: fp32 [128 lanes][128] at columns 128 b
-constexpr uint32_t TM_P = 256;    // P buffer b: fp16 pairs [128 lanes][64] at columns 256 + 64 b
-constexpr uint32_t TM_O = 384;    // O: fp32 [128 lanes][D]
-// log2 of the largest unnormalised weight.  A wide bound keeps rescales (a
-// wait for the previous PV, O and the sums rescaled) rare even when the
-// logits of a row spread over many octaves; P = weight * s_v * 2^c still fits
-// fp16 because the per-head factor 2^c shrinks by the same number of octaves.
-constexpr int kLazyLog2 = 14;
+constexpr uint32_t TM_P = 256;    // P: fp16 pairs [128 lanes][64]
+constexpr uint32_t TM_L = 352;    // L: fp32 [128 lanes][16] (columns 0, 1: hi and lo sums) of 32 kept
+constexpr uint32_t TM_O = 384;    // O: fp32 [128 lanes][D], right after L's 32 columns
+constexpr int UN = 16;            // columns of the row-sum MMA
+// log2 of the scale floor under the head's largest V scale (and of the
+// largest u, which must stay inside fp16)
+constexpr int kFloorLog2 = 15;
+// log2 of the largest unnormalised weight.  A wider bound makes rescales (a
+// wait for the previous PV, O and L rescaled) rarer, but the per-head factor
+// 2^c that keeps every P = weight * w * 2^c below fp16's maximum then puts
+// the row's largest P lower, and more of its small weights into fp16
+// subnormals or zero.  Those weights are lost to L as well as to O, and with
+// many of them that changes the output.  Right after a row's maximum is set,
+// its largest P is 2^(14 - kLazyLog2 - kHeadroom) = 2^0 (times w 2^c in
+// [1, 2)), so weights down to 2^-14 of it stay normal.
+constexpr int kLazyLog2 = 10;
 constexpr float kLazyRescale = (float)kLazyLog2;
 // A running maximum is set this many octaves above the tile maximum that sets
 // it (weights then start at most 2^-4), so later tiles may exceed the observed
@@ -81,14 +101,20 @@ struct AttnLayout {
   static constexpr int K0 = Q + BM * D;                  // NSTAGE x e4m3 [BN][D]
   static constexpr int V0 = K0 + NSTAGE * BN * D;        // NSTAGE x e4m3 [BN][D]
   static constexpr int VH0 = V0 + NSTAGE * BN * D;       // 2 x fp16 [BN][D], MN-major swizzled
-  static constexpr int SC0 = VH0 + 2 * BN * D * 2;       // NSC x fp32 {s_k [BN], s_v [BN]}
-  static constexpr int ML = SC0 + NSC * 2 * BN * 4;      // fp32 row sums [BM]
-  static constexpr int BAR = ML + BM * 4;
-  static constexpr int NBAR = 2 * NSTAGE + 2 * NSC + 9 + 4;
+  static constexpr int U0 = VH0 + 2 * BN * D * 2;        // 2 x fp16 [UN][BN], K-major, 128-byte swizzle
+  static constexpr int SC0 = U0 + 2 * UN * BN * 2;       // NSC x fp32 {s_k [BN], s_v [BN]}
+  static constexpr int BAR = SC0 + NSC * 2 * BN * 4;
+  static constexpr int NBAR = 2 * NSTAGE + 2 * NSC + 9;
   static constexpr int MISC = BAR + NBAR * 8;
   static constexpr int BYTES = MISC + 64;
   static constexpr int ALLOC = BYTES + 1024;             // slack for 1024-byte alignment
 };
+
+// byte offset of the fp16 element (row n, slot k) of a u tile: two 64-slot
+// atoms of [UN rows][128 bytes], 128-byte swizzle
+__device__ __forceinline__ int u_elem(int n, int k) {
+  return (k >> 6) * (UN * 128) + n * 128 + ((((k & 63) >> 3) ^ (n & 7)) << 4) + (k & 7) * 2;
+}
 
 // byte offset of 16-byte chunk c of row r in a K-major tile whose rows are
 // D bytes (D = 128: 128-byte swizzle; D = 64: 64-byte swizzle)
@@ -123,18 +149,17 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
   uint64_t* kv_full = bars;                     // [NSTAGE] K, V codes landed
   uint64_t* kv_empty = kv_full + NSTAGE;        // [NSTAGE] K read by QK, V widened
   uint64_t* sc_full = kv_empty + NSTAGE;        // [NSC] scales landed
-  uint64_t* sc_empty = sc_full + NSC;           // [NSC] the tile's softmax is done
+  uint64_t* sc_empty = sc_full + NSC;           // [NSC] the tile's softmax and u columns are done
   uint64_t* s_full = sc_empty + NSC;            // [2] QK done into S buffer b
-  uint64_t* p_full = s_full + 2;                // [2] P in buffer b, S buffer b read
-  uint64_t* pv_done = p_full + 2;               // [2] PV from P buffer b done
-  uint64_t* vh_full = pv_done + 2;              // [2] fp16 V buffer b written
+  uint64_t* p_full = s_full + 2;                // [2] P of tile parity b stored, S buffer b read
+  uint64_t* pv_done = p_full + 2;               // [2] PV and row sums of tile parity b done
+  uint64_t* vh_full = pv_done + 2;              // [2] fp16 V buffer b and u tile b written
   uint64_t* q_full = vh_full + 2;               // query tile + range factor
-  uint64_t* ml_xchg = q_full + 1;               // [4] per lane quarter
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + LY::MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + LY::MISC + 4);
   int* maxsv_bits = reinterpret_cast<int*>(sm + LY::MISC + 8);
   float* cv_smem = reinterpret_cast<float*>(sm + LY::MISC + 12);   // log2 of the per-head weight factor
-  float* lrow = reinterpret_cast<float*>(sm + LY::ML);
+  float* floor_smem = reinterpret_cast<float*>(sm + LY::MISC + 16);  // the per-head scale floor
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -150,7 +175,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
     }
     for (int i = 0; i < NSC; ++i) {
       mbar_init(&sc_full[i], 1);
-      mbar_init(&sc_empty[i], SOFT_WARPS);
+      mbar_init(&sc_empty[i], SOFT_WARPS + CONV_WARPS);   // the softmax, the u columns
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
@@ -159,7 +184,6 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       mbar_init(&vh_full[i], CONV_WARPS);
     }
     mbar_init(q_full, 1 + CONV_WARPS);   // the query tile's TMA, the widening warps (range factor)
-    for (int i = 0; i < 4; ++i) mbar_init(&ml_xchg[i], 2);
     *abort_flag = 0;
     *maxsv_bits = 0;
     fence_mbar_init();
@@ -207,23 +231,22 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
     const int c4 = lane & 3;
     const int r4 = lane >> 2;
     const uint32_t lanes = (uint32_t)(32 * quarter + 16 * hf) << 16;
-    const uint32_t o_addr = tmem + lanes + TM_O;
+    const uint32_t lo_addr = tmem + lanes + TM_L;   // L's 32 columns, then O
     constexpr float kRowC = (D == 128 ? 0.08838834764831845f : 0.125f) * 1.4426950408889634f;
     float rq[2], m_run[2];
-    float2 lsum[2];
 #pragma unroll
     for (int sb = 0; sb < 2; ++sb) {
       const int qrow = qt * BM + 32 * quarter + 16 * hf + r4 + 8 * sb;
       const float sq = qrow < n_q ? rv.q_scale[(size_t)h * rv.Q_pad + qrow] : 0.0f;
       rq[sb] = sq > 0.0f ? sq * kRowC : 1.0f;
       m_run[sb] = -INFINITY;
-      lsum[sb] = make_float2(0.0f, 0.0f);
     }
     bool ok = mbar_wait(q_full, 0, abort_flag);
     const float log2cv = *cv_smem;
+    const float sfloor = *floor_smem;
     // Raise the running maxima of rows a and b to mn0, mn1 at tile j > 0:
-    // O holds rows weighted by exp2(-m_run), so once PV_{j-1} (and so every
-    // earlier PV) is done they are brought to exp2(-m_new), with the sums.
+    // O and L hold rows weighted by exp2(-m_run), so once PV_{j-1} (and so
+    // every earlier PV and row sum) is done they are brought to exp2(-m_new).
     // Returns the factors 2^(m_old - m_new); false if the wait gave up.
     auto raise_max = [&](int j, float mn0, float mn1, float& al0, float& al1) -> bool {
       al0 = 1.0f;
@@ -234,9 +257,9 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         al0 = ex2f(m_run[0] - mn0);
         al1 = ex2f(m_run[1] - mn1);
 #pragma unroll 1
-        for (int c0 = 0; c0 < D; c0 += 32) {
+        for (int c0 = 0; c0 < 32 + D; c0 += 32) {
           uint32_t o[16];
-          tmem_ld_16x256b_x4(o_addr + c0, o);
+          tmem_ld_16x256b_x4(lo_addr + c0, o);
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             o[4 * k] = __float_as_uint(__uint_as_float(o[4 * k]) * al0);
@@ -244,10 +267,8 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
             o[4 * k + 2] = __float_as_uint(__uint_as_float(o[4 * k + 2]) * al1);
             o[4 * k + 3] = __float_as_uint(__uint_as_float(o[4 * k + 3]) * al1);
           }
-          tmem_st_16x256b_x4(o_addr + c0, o);
+          tmem_st_16x256b_x4(lo_addr + c0, o);
         }
-        lsum[0] = mul2(lsum[0], make_float2(al0, al0));
-        lsum[1] = mul2(lsum[1], make_float2(al1, al1));
       }
       m_run[0] = mn0;
       m_run[1] = mn1;
@@ -273,7 +294,6 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       // maximum formed, raised, O and the sums rescaled, and the tile
       // recomputed from S, which stays in TMEM until this tile's end.
       uint32_t pk[32];
-      float2 la = make_float2(0.0f, 0.0f), lb = la;
       for (int pass = (j == 0 ? 1 : 0); pass < 2; ++pass) {
         uint32_t xr[64];
         tmem_ld_16x256b_x16(s_addr, xr);
@@ -376,19 +396,11 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
             x[4 * k + 3] = eb.y;
           }
         }
-        float2 la0 = make_float2(0.0f, 0.0f), la1 = la0, lb0 = la0, lb1 = la0;
-#pragma unroll
-        for (int k = 0; k < 16; k += 2) {
-          la0 = add2(la0, make_float2(x[4 * k], x[4 * k + 1]));
-          lb0 = add2(lb0, make_float2(x[4 * k + 2], x[4 * k + 3]));
-          la1 = add2(la1, make_float2(x[4 * k + 4], x[4 * k + 5]));
-          lb1 = add2(lb1, make_float2(x[4 * k + 6], x[4 * k + 7]));
-        }
-        la = add2(la0, la1);
-        lb = add2(lb0, lb1);
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
-          const float2 sv = *reinterpret_cast<const float2*>(svp + 8 * k);
+          float2 sv = *reinterpret_cast<const float2*>(svp + 8 * k);
+          sv.x = fmaxf(sv.x, sfloor);
+          sv.y = fmaxf(sv.y, sfloor);
           const float2 pa2 = mul2(make_float2(x[4 * k], x[4 * k + 1]), sv);
           const float2 pb2 = mul2(make_float2(x[4 * k + 2], x[4 * k + 3]), sv);
           pk[2 * k] = cvt_f16x2(pa2.x, pa2.y);
@@ -397,15 +409,13 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         break;
       }
       if (!ok) break;
-      lsum[0] = add2(lsum[0], la);
-      lsum[1] = add2(lsum[1], lb);
-      // P buffer b is free once PV_{j-2} is done
-      if (j >= 2 && !mbar_wait(&pv_done[b], ((j - 2) >> 1) & 1, abort_flag)) {
+      // P is free once PV_{j-1} (and its row sums) have read it
+      if (j >= 1 && !mbar_wait(&pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      tmem_st_16x128b_x16(tmem + lanes + TM_P + 64 * b, pk);
+      tmem_st_16x128b_x16(tmem + lanes + TM_P, pk);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
@@ -414,26 +424,17 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       }
     }
     // ======================================================== output
-    // Each row's sum is spread over the four threads that share it.  The two
-    // warps of a lane quarter publish the sums of their rows in shared
-    // memory; each then writes half of the output columns of the quarter's
-    // 32 rows, one row per thread (thread t <-> lane 32*quarter + t).
-#pragma unroll
-    for (int sb = 0; sb < 2; ++sb) {
-      float l = lsum[sb].x + lsum[sb].y;
-      l += __shfl_xor_sync(0xFFFFFFFFu, l, 1);
-      l += __shfl_xor_sync(0xFFFFFFFFu, l, 2);
-      if (c4 == 0) lrow[32 * quarter + 16 * hf + r4 + 8 * sb] = l;
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&ml_xchg[quarter]);
-    ok = ok && mbar_wait(&ml_xchg[quarter], 0, abort_flag);
+    // Both warps of a lane quarter read the row sums of its 32 rows, one row
+    // per thread (thread t <-> lane 32*quarter + t), and each writes half of
+    // the output columns.
     const int r = 32 * quarter + lane;
-    const float l_row = lrow[r];
     ok = ok && mbar_wait(&pv_done[(T - 1) & 1], ((T - 1) >> 1) & 1, abort_flag);
     if (ok) {
       tc_fence_after();
-      const float inv_l = 1.0f / l_row;
+      uint32_t lr[2];
+      tmem_ld_32x32b_x2(tmem + ((uint32_t)(32 * quarter) << 16) + TM_L, lr);
+      const float L = __uint_as_float(lr[0]) + __uint_as_float(lr[1]) * 0x1p-11f;
+      const float inv_l = 1.0f / ldexpf(L, (int)log2cv);
       const int qi = qt * BM + r;
       const uint32_t row_o = tmem + ((uint32_t)(32 * quarter) << 16) + TM_O;
       uint8_t* orow = static_cast<uint8_t*>(out) + ((size_t)qi * H + h) * (size_t)D * (out_f32 ? 4 : 2);
@@ -492,24 +493,44 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       if (ct == 0) {
         const float m = __int_as_float(*maxsv_bits);
         // weights reach 2^kLazyLog2 * 2^c; with c = 14 - kLazyLog2 -
-        // floor(log2 max s_v) every P = weight * s_v stays below 2^15 (fp16
-        // max 65504)
+        // floor(log2 max s_v) every P = weight * w stays below 2^15 (fp16
+        // max 65504), w = max(s_v, floor) <= max(max s_v, 2^-c)
         int c = m > 0.0f ? 14 - kLazyLog2 - ilogbf(m) : 0;
         c = c < -64 ? -64 : (c > 64 ? 64 : c);
         *cv_smem = (float)c;
+        // the scale floor: u = 2^-c / max(s_v, floor) <= 2^kFloorLog2
+        *floor_smem = ldexpf(fmaxf(m, ldexpf(1.0f, -c)), -kFloorLog2);
       }
       asm volatile("bar.sync 1, %0;" ::"n"(CONV_THREADS) : "memory");
       __syncwarp();
       if (lane == 0) mbar_arrive(q_full);
     }
 
+    // u tiles: rows 2 .. UN-1 stay zero; rows 0 and 1 are written per tile
+    for (int i = ct; i < 2 * UN * BN * 2 / 16; i += CONV_THREADS)
+      reinterpret_cast<uint4*>(sm + LY::U0)[i] = make_uint4(0, 0, 0, 0);
+    const float cscale = ldexpf(1.0f, -(int)*cv_smem);   // 2^-c
+    const float sfloor = *floor_smem;
+
     constexpr int CH = D / 16;  // 16-byte e4m3 chunks per slot row
     for (int u = 0; u < T; ++u) {
       const int st = u % NSTAGE;
+      const int sc = u % NSC;
       const int b = u & 1;
       if (!mbar_wait<true>(&kv_full[st], (u / NSTAGE) & 1, abort_flag)) break;
-      // fp16 V buffer b is free once PV_{u-2} is done
+      // fp16 V buffer b and u tile b are free once PV_{u-2} is done
       if (u >= 2 && !mbar_wait<true>(&pv_done[b], ((u - 2) >> 1) & 1, abort_flag)) break;
+      if (!mbar_wait<true>(&sc_full[sc], (u / NSC) & 1, abort_flag)) break;
+      {
+        // slot ct of the tile: u = 2^-c / max(s_v, floor) as fp16 u_hi + u_lo * 2^-11
+        const float sv = reinterpret_cast<const float*>(sm + LY::SC0 + sc * 2 * BN * 4)[BN + ct];
+        const float uv = __fdiv_rn(cscale, fmaxf(sv, sfloor));
+        const __half hi = __float2half_rn(uv);
+        const __half lo = __float2half_rn((uv - __half2float(hi)) * 2048.0f);
+        uint8_t* ut = sm + LY::U0 + b * UN * BN * 2;
+        *reinterpret_cast<__half*>(ut + u_elem(0, ct)) = hi;
+        *reinterpret_cast<__half*>(ut + u_elem(1, ct)) = lo;
+      }
       const uint8_t* vsrc = sm + LY::V0 + st * BN * D;
       uint8_t* vdst = sm + LY::VH0 + b * BN * D * 2;
       // eight consecutive threads take the same chunk of eight consecutive
@@ -542,6 +563,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       if (lane == 0) {
         mbar_arrive(&vh_full[b]);
         mbar_arrive(&kv_empty[st]);
+        mbar_arrive(&sc_empty[sc]);
       }
     }
   } else if (warp == WARP_TMA) {
@@ -565,10 +587,11 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
   } else {
     // ======================================================== MMA issue
     // QK_0, QK_1, then per tile j, once the softmax of tile j is done: QK_{j+2}
-    // into the S buffer it has finished reading, then PV_j.
+    // into the S buffer it has finished reading, then PV_j and its row sums.
     if (lane == 0) {
       constexpr uint32_t idesc_qk = make_idesc(0, 0, 0, 0, BM, BN);   // e4m3 x e4m3, both K-major
       constexpr uint32_t idesc_pv = make_idesc(0, 0, 0, 1, BM, D);    // f16 x f16, V MN-major
+      constexpr uint32_t idesc_l = make_idesc(0, 0, 0, 0, BM, UN);    // f16 x f16, u K-major
       bool ok = mbar_wait(q_full, 0, abort_flag);
       const uint32_t q_addr = smem_u32(sm + LY::Q);
       auto issue_qk = [&](int u) -> bool {
@@ -593,10 +616,17 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         tc_fence_after();
         if (j + 2 < T && !issue_qk(j + 2)) break;
         const uint32_t va = smem_u32(sm + LY::VH0 + b * BN * D * 2);
+        const uint32_t ua = smem_u32(sm + LY::U0 + b * UN * BN * 2);
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
-          mma_f16_ts(tmem + TM_O, tmem + TM_P + 64 * b + kk * 8, make_sdesc_sw128(va + kk * 16 * 128, BN * 128, 1024),
+          mma_f16_ts(tmem + TM_O, tmem + TM_P + kk * 8, make_sdesc_sw128(va + kk * 16 * 128, BN * 128, 1024),
                      idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+        // 16 slots (32 bytes) per MMA; four per 64-slot atom
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk)
+          mma_f16_ts(tmem + TM_L, tmem + TM_P + kk * 8,
+                     make_sdesc_sw128(ua + (kk >> 2) * (UN * 128) + (kk & 3) * 32, 16, 1024), idesc_l,
+                     (j > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&pv_done[b]);
       }
     }

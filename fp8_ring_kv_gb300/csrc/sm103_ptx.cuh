@@ -281,6 +281,16 @@ __device__ __forceinline__ void tmem_st_16x128b_x16(uint32_t taddr, const uint32
       : "memory");
 }
 
+// 32x32b.x2: thread t <-> lane t, register i <-> column i.
+__device__ __forceinline__ void tmem_ld_32x32b_x2(uint32_t taddr, uint32_t (&r)[2]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0,%1}, [%2];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1])
+      : "r"(taddr)
+      : "memory");
+}
+
 // Two 32x32b.x16 loads (thread t <-> lane t, register i <-> column i) and
 // the wait, in one statement.
 __device__ __forceinline__ void tmem_ld2_32x32b_x16(uint32_t a0, uint32_t a1, uint32_t (&r)[16], uint32_t (&q)[16]) {

@@ -191,7 +191,8 @@ int kvring_reset_positions(kvring* r, int32_t d, kvring_stream stream);
  * query scratch); out = softmax(q.k / sqrt(D)) v over slots
  * 0 .. n_valid-1 with dequantised q, k and v, no mask.  Scores come from FP8
  * tensor-core products with fp32 accumulation; the softmax weights are
- * rounded to fp16 for the weighted sum of V.
+ * rounded to fp16 for the weighted sum of V, and the row sums that normalise
+ * it are taken from the same fp16 weights (so their rounding cancels).
  */
 int kvring_attend(kvring* r, const void* q, const int32_t* q_pos, int32_t n_q, void* out,
                   kvring_stream stream);

@@ -16,12 +16,14 @@ Every function is written from the plain definition of what it computes:
 
 * ``e4m3``  -- the OCP E4M3 ("FN") code table and a round-to-nearest-even,
   saturating encoder.
-* ``quant`` -- per-token-per-head absmax quantisation to e4m3.
+* ``quant`` -- per-token-per-head absmax quantisation to e4m3, and the
+  paper's per-head scales fixed once per session (margin x amax, saturating).
 * ``rope``  -- RoPE frequencies, the fp32 cos/sin tables, RoPE in fp32 and in
   fp64, the delta rotation R(-d).
 * ``ring``  -- the ring of slots with its write position, the optional global
-  slots ahead of it (written once, never rotated), and the whole call
-  sequence (write_global / write / reset_positions / attend).
+  slots ahead of it (written once, never rotated), the scale mode (per token,
+  or per head fixed by ``calibrate``), and the whole call sequence
+  (write_global / write / calibrate / reset_positions / attend).
 * ``attention`` -- dense softmax attention in fp64.
 
 Parity pins (tests/test_oracle_*.py) tie each function to something other than

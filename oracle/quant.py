@@ -50,3 +50,34 @@ def dequantize_rows_f64(codes, scale):
     """Exact dequantisation in fp64 (the product of an e4m3 value and an fp32
     scale is exact in fp64)."""
     return e4m3.decode(codes) * np.asarray(scale, dtype=np.float64)[..., None]
+
+
+# --- per-head scales fixed once per session ------------------------------------
+# The paper's own scheme (§4.3 "FP8 at write"; Appendix G): one scale per
+# (cache, head) for K and one for V, set once per session from the absolute
+# maximum of what the first steps wrote, times a margin of 1.5; later values
+# beyond the range saturate, and a position reset keeps the scale and clamps.
+#
+#     a     = fl32(margin * amax)
+#     scale = fl32(a / 448),  inv = fl32(448 / a)       (0 and 0 when a = 0)
+#     code_i = e4m3_rn_satfinite(fl32(x_i * inv))       (+0 when inv = 0)
+
+def static_scale(amax, margin=1.5):
+    """Per-head amax (float32 [...]) -> (scale, inv), float32 [...]."""
+    amax = np.asarray(amax, dtype=np.float32)
+    a = (np.float32(margin) * amax).astype(np.float32)
+    zero = a == 0
+    safe = np.where(zero, np.float32(1.0), a).astype(np.float32)
+    scale = np.where(zero, np.float32(0.0), (safe / F32_448).astype(np.float32)).astype(np.float32)
+    inv = np.where(zero, np.float32(0.0), (F32_448 / safe).astype(np.float32)).astype(np.float32)
+    return scale, inv
+
+
+def quantize_rows_fixed(x, inv):
+    """x: float32 [..., D]; inv: float32 [...] (one per row, broadcast) ->
+    codes uint8 [..., D], saturating at +-448."""
+    x = np.asarray(x, dtype=np.float32)
+    inv = np.asarray(inv, dtype=np.float32)
+    y = (x * inv[..., None]).astype(np.float32)
+    codes = e4m3.encode_rn_satfinite(y)
+    return np.where((inv == 0)[..., None], np.uint8(0), codes).astype(np.uint8)

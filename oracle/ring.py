@@ -31,9 +31,17 @@ ring above.  A ring of six latent frames (Appendix G) is the window ring with
 W = 6 x 757 and writes of 757 tokens: every frame then fills whole,
 consecutive slots and the seventh frame replaces the first.
 
-Scales are per (token, head), recomputed at write and at reset (absmax, see
-``quant``); this replaces the paper's per-(layer, head) scales calibrated once
-per session.
+Scales (``scale_mode``).  "token" (the default): one scale per (token,
+head), recomputed at write and at reset (absmax, see ``quant``).  "static":
+the paper's own scheme (§4.3 "FP8 at write"; Appendix G) -- until
+``calibrate`` the ring quantises per token and records each head's absolute
+maximum of the K (after RoPE) and V values written; ``calibrate(margin)``
+sets one K and one V scale per head from those maxima times the margin,
+re-quantises the slots written so far with them (from their dequantised
+values, fp32), and from then on writes use them, saturating, and a reset
+keeps them and clamps (saturates) the rotated keys.  A reset before the
+calibration is refused: the paper calibrates on entering the seventh step and
+resets every 42.
 """
 import numpy as np
 
@@ -42,7 +50,7 @@ from .attention import attend_f64
 
 
 class OracleRing:
-    def __init__(self, heads, head_dim, n_slots, axis_dims, base=10000.0, n_global=0):
+    def __init__(self, heads, head_dim, n_slots, axis_dims, base=10000.0, n_global=0, scale_mode="token"):
         if sum(axis_dims) != head_dim or any(d % 2 for d in axis_dims):
             raise ValueError("axis_dims must be even and sum to head_dim")
         self.H, self.D, self.S = int(heads), int(head_dim), int(n_slots)
@@ -51,6 +59,12 @@ class OracleRing:
             raise ValueError("n_global must leave at least one window slot")
         self.W = self.S - self.G
         self.globals_written = False
+        if scale_mode not in ("token", "static"):
+            raise ValueError("scale_mode is 'token' or 'static'")
+        self.scale_mode = scale_mode
+        self.static = None                                # (k_scale, k_inv, v_scale, v_inv), [H] each
+        self.cal_amax_k = np.zeros(int(heads), np.float32)
+        self.cal_amax_v = np.zeros(int(heads), np.float32)
         self.axis_dims = tuple(int(d) for d in axis_dims)
         self.base = float(base)
         self.k_codes = np.zeros((self.H, self.S, self.D), np.uint8)
@@ -65,9 +79,22 @@ class OracleRing:
         return self.G + (self.wp + np.arange(n_new)) % self.W
 
     def _store(self, k, v, pos, slots):
-        """RoPE on K (fp32), absmax e4m3 of K and V, into ``slots``."""
-        kc, ks = quant.quantize_rows(rope.rope_f32(k, pos, self.axis_dims, self.base))
-        vc, vs = quant.quantize_rows(v)
+        """RoPE on K (fp32), e4m3 of K and V (per-token absmax scales, or the
+        fixed per-head ones once calibrated), into ``slots``."""
+        kr = rope.rope_f32(k, pos, self.axis_dims, self.base)
+        if self.static is None:
+            kc, ks = quant.quantize_rows(kr)
+            vc, vs = quant.quantize_rows(v)
+            if self.scale_mode == "static":
+                self.cal_amax_k = np.maximum(self.cal_amax_k, np.abs(kr).max(axis=(0, 2)))
+                self.cal_amax_v = np.maximum(self.cal_amax_v, np.abs(v).max(axis=(0, 2)))
+        else:
+            k_scale, k_inv, v_scale, v_inv = self.static
+            n = kr.shape[0]
+            kc = quant.quantize_rows_fixed(kr, np.broadcast_to(k_inv, (n, self.H)))
+            vc = quant.quantize_rows_fixed(v, np.broadcast_to(v_inv, (n, self.H)))
+            ks = np.broadcast_to(k_scale, (n, self.H))
+            vs = np.broadcast_to(v_scale, (n, self.H))
         self.k_codes[:, slots, :] = np.transpose(kc, (1, 0, 2))
         self.v_codes[:, slots, :] = np.transpose(vc, (1, 0, 2))
         self.k_scale[:, slots] = ks.T
@@ -104,20 +131,44 @@ class OracleRing:
         self.n_valid = self.G
         return slots
 
+    # -- calibration (scale_mode "static") --------------------------------------
+    def calibrate(self, margin=1.5):
+        """Fix the per-head K and V scales from the recorded maxima times
+        ``margin`` and re-quantise the valid slots with them."""
+        if self.scale_mode != "static" or self.static is not None:
+            raise ValueError("calibrate once, on a ring with scale_mode 'static'")
+        if self.n_valid == 0:
+            raise ValueError("calibrate after the first write")
+        k_scale, k_inv = quant.static_scale(self.cal_amax_k, margin)
+        v_scale, v_inv = quant.static_scale(self.cal_amax_v, margin)
+        n = self.n_valid
+        for codes, scales, sc, iv in ((self.k_codes, self.k_scale, k_scale, k_inv),
+                                      (self.v_codes, self.v_scale, v_scale, v_inv)):
+            x = quant.dequantize_rows(codes[:, :n], scales[:, :n])
+            codes[:, :n] = quant.quantize_rows_fixed(x, np.broadcast_to(iv[:, None], (self.H, n)))
+            scales[:, :n] = sc[:, None]
+        self.static = (k_scale, k_inv, v_scale, v_inv)
+
     # -- reset ---------------------------------------------------------------
     def reset_positions(self, d):
         """Rotate every valid window key by R(-d) on the temporal axis
         (axis 0), in fp32, and re-quantise it with a fresh absmax scale.
         Global keys are not touched."""
+        if self.scale_mode == "static" and self.static is None:
+            raise ValueError("a ring with scale_mode 'static' is calibrated before its first reset")
         lo, hi = self.G, self.n_valid
         if hi <= lo:
             return
         c, s = rope.delta_cos_sin_f32(d, self.axis_dims[0], self.base)
         k = quant.dequantize_rows(self.k_codes[:, lo:hi], self.k_scale[:, lo:hi])
         k = rope.rotate_temporal_f32(k, c, s, self.axis_dims[0])
-        codes, scale = quant.quantize_rows(k)
+        if self.static is None:
+            codes, scale = quant.quantize_rows(k)
+            self.k_scale[:, lo:hi] = scale
+        else:
+            # the same per-head scale; rotated values beyond the range saturate
+            codes = quant.quantize_rows_fixed(k, np.broadcast_to(self.static[1][:, None], (self.H, hi - lo)))
         self.k_codes[:, lo:hi] = codes
-        self.k_scale[:, lo:hi] = scale
 
     # -- attend --------------------------------------------------------------
     def quantized_queries(self, q, q_pos):

@@ -22,6 +22,11 @@ cpu_baseline   the oracle on a bounded sample, extrapolated, on host cores
 Multi-GPU: one process per GPU under torchrun; each rank runs its own rings
 (the path shards by ring / head with no exchange): weak scaling.
 
+``--layout paper`` runs the same step on the paper's own cache layout: 1,246
+global slots written once, then a window ring of 6 x 757 slots; the write
+goes into the window, the reset rotates the 4,542 window keys only, the
+attention reads all 5,788 slots.
+
 ``--impl reference`` times the oracle (numpy) instead, on host cores, with a
 per-step sample sized so the whole run stays within a few minutes.
 """
@@ -46,10 +51,14 @@ H, D, S, N = 24, 128, synth.SLOTS, synth.NEW_TOKENS
 RESET_D = synth.RESET_PERIOD * N
 METRIC = "fp8_ring_attn calls/s + write/rerotate HBM GB/s at 5788 slots, 757 new"
 WORKLOAD = "single attention call at the paper's shape: 24 heads x 128, 5788-slot FP8 ring, 757 new tokens"
+WORKLOAD_PAPER = ("single attention call on the paper's cache layout: 24 heads x 128, 1246 global slots + "
+                  "a 6 x 757-slot FP8 window ring, 757 new tokens")
 
 # algorithmic work per launch: bytes each kernel must move, flops of the two contractions
 WRITE_BYTES = N * H * (6 * D + 8) + 4 * N * 1          # bf16 K,V in; e4m3 K,V + 2 fp32 scales out; positions
 REROT_BYTES = S * H * (2 * D + 8)                      # K codes + K scale, read and written
+G = synth.GLOBAL_SLOTS                                 # --layout paper: global slots ahead of the window
+REROT_BYTES_PAPER = (S - G) * H * (2 * D + 8)          # the window keys only
 ATTN_FLOPS = 4 * N * S * D * H                         # QK^T and PV
 # kernels per step: ring_kv_write, delta_rerotate, and the attend call's two
 # (query RoPE + e4m3, then fp8_ring_attn)
@@ -142,10 +151,13 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- the GPU arm
-def make_rings(n_rings, dev):
+def make_rings(n_rings, dev, layout="ring"):
     from fp8_ring_kv_gb300.kvring import KVRing, KVRING_OUT_BF16
     wl = synth.single()
     shape = wl.shape
+    if layout == "paper":
+        # positions: globals at -G .. -1, window prefill at 0 .. S-G-1, new tokens at S .. S+N-1
+        shape = synth.Shape(H, D, S, (D,), (-G,), (G + S + N,), n_global=G)
     ops = list(wl.ops)
     prefill = ops[0]
     rings, inputs = [], []
@@ -156,7 +168,11 @@ def make_rings(n_rings, dev):
     ch = synth.outlier_channels(synth.rng(1), H, D)
     for r in range(n_rings):
         ring = KVRing.from_shape(shape, KVRING_OUT_BF16)
-        ring.write(kp, vp, pp)
+        if layout == "paper":
+            ring.write_global(kp[:G], vp[:G], pp[:G] - G)
+            ring.write(kp[G:], vp[G:], pp[:S - G])
+        else:
+            ring.write(kp, vp, pp)
         g = synth.rng(1, 100 + r)
         k = synth.normal_bf16(g, (N, H, D), ch).to(dev)
         v = synth.normal_bf16(g, (N, H, D), ch).to(dev)
@@ -207,7 +223,8 @@ def run_gpu(args, rank, world, local_rank):
     from fp8_ring_kv_gb300 import kvring
     kvring.load()
     R = args.rings
-    rings, inputs = make_rings(R, dev)
+    rings, inputs = make_rings(R, dev, args.layout)
+    rerot_bytes = REROT_BYTES_PAPER if args.layout == "paper" else REROT_BYTES
 
     full = capture(lambda: [step(rings[r], inputs[r]) for r in range(R)])
     singles = [capture(lambda r=r: step(rings[r], inputs[r])) for r in range(R)]
@@ -245,7 +262,7 @@ def run_gpu(args, rank, world, local_rank):
     kern = {}
     for name, fn, work, unit in (
             ("ring_kv_write", lambda r: rings[r].write(inputs[r][0], inputs[r][1], inputs[r][3]), WRITE_BYTES, "GB/s"),
-            ("delta_rerotate", lambda r: rings[r].reset_positions(RESET_D), REROT_BYTES, "GB/s"),
+            ("delta_rerotate", lambda r: rings[r].reset_positions(RESET_D), rerot_bytes, "GB/s"),
             ("fp8_ring_attn", lambda r: rings[r].attend(inputs[r][2], inputs[r][3], out=inputs[r][4]), ATTN_FLOPS,
              "TFLOP/s")):
         g = capture(lambda fn=fn: [fn(r) for r in range(R)])
@@ -407,6 +424,8 @@ def main():
     ap.add_argument("--rings", type=int, default=8)
     ap.add_argument("--e2e-steps", type=int, default=2000)
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
+    ap.add_argument("--layout", default="ring", choices=["ring", "paper"],
+                    help="ring: all 5,788 slots one ring; paper: 1,246 global slots + a 6 x 757 window ring")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
@@ -437,7 +456,7 @@ def main():
     dist_init(world, "nccl")
     res = run_gpu(args, rank, world, local_rank)
     cpu = None
-    if rank == 0 and world == 1 and args.cpu_budget > 0:
+    if rank == 0 and world == 1 and args.cpu_budget > 0 and args.layout == "ring":
         smp = OracleSample(heads=2)
         t0 = time.time()
         rate, n = smp.run(1, budget_s=args.cpu_budget)
@@ -453,8 +472,10 @@ def main():
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(res["ms_per_step"], 5),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3/f16/f32",
             "data": "synthetic",
-            "config": {"workload": WORKLOAD, "heads": H, "head_dim": D, "slots": S, "new_tokens": N,
-                       "step": "ring_kv_write(757) + delta_rerotate(5788 slots) + fp8_ring_attn(757 q)",
+            "config": {"workload": WORKLOAD if args.layout == "ring" else WORKLOAD_PAPER,
+                       "heads": H, "head_dim": D, "slots": S, "new_tokens": N,
+                       "step": "ring_kv_write(757) + delta_rerotate(%d slots) + fp8_ring_attn(757 q)"
+                               % (S if args.layout == "ring" else S - G),
                        "rings_cycled": args.rings,
                        "l2": f"cold by construction: {args.rings} rings x ~50 MB cycled (> 129 MB L2)",
                        "graphs": "steps replayed from CUDA graphs", "parallelism": f"replicas x{world}"},

@@ -13,7 +13,11 @@ constexpr int kMaxAxes = 3;
 constexpr float kE4m3Max = 448.0f;
 
 // state words at the start of the workspace
-enum : int { ST_WP = 0, ST_NVALID = 1, ST_ERR = 2, ST_DONE = 3, ST_WORDS = 64 };
+// ST_STATIC: 1 once a ring with per-head fixed scales has been calibrated
+enum : int { ST_WP = 0, ST_NVALID = 1, ST_ERR = 2, ST_DONE = 3, ST_STATIC = 4, ST_WORDS = 64 };
+// per-head fixed scales, fp32 [6][H]: the recorded maxima of K and V, then
+// (scale, inv) of K and of V
+enum : int { STAT_AMAX_K = 0, STAT_AMAX_V = 1, STAT_K_SCALE = 2, STAT_K_INV = 3, STAT_V_SCALE = 4, STAT_V_INV = 5 };
 enum : int { DEVERR_POS_RANGE = 1, DEVERR_EMPTY = 2, DEVERR_TIMEOUT = 4 };
 
 // Device view of one ring, passed by value to every kernel.
@@ -32,6 +36,8 @@ struct RingView {
   float* q_scale;                 // query scratch: fp32 [H][Q_pad]
   int32_t H, D, S, S_pad, n_axes, Q_pad;
   int32_t G;                      // global slots 0 .. G-1; the window ring is slots G .. S-1
+  float* stat;                    // per-head fixed scales [6][H] (STAT_*)
+  int32_t scale_mode;             // 0: per (token, head) scales; 1: per head, fixed by calibration
 };
 
 // ---------------------------------------------------------------- numerics

@@ -31,6 +31,7 @@ struct kvring {
   // call order, tracked on the host (the calls are enqueued in host order)
   bool globals_written;
   bool window_written;
+  bool calibrated;
 };
 
 namespace {
@@ -47,7 +48,7 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct Layout {
-  size_t state, rope[3], k_codes, v_codes, k_scale, v_scale, q_codes, q_scale, total;
+  size_t state, rope[3], k_codes, v_codes, k_scale, v_scale, stat, q_codes, q_scale, total;
   int s_pad, q_pad;
 };
 
@@ -68,6 +69,7 @@ bool check_config(const kvring_config* c) {
   if (c->out_dtype != KVRING_OUT_BF16 && c->out_dtype != KVRING_OUT_F32) return false;
   if (c->max_queries < 1 || c->max_queries > (1 << 20)) return false;
   if (c->n_global < 0 || c->n_global >= c->n_slots) return false;
+  if (c->scale_mode != KVRING_SCALES_TOKEN && c->scale_mode != KVRING_SCALES_STATIC) return false;
   return true;
 }
 
@@ -90,6 +92,8 @@ Layout layout_of(const kvring_config* c) {
   off = round_up(off + H * L.s_pad * sizeof(float), 1024);
   L.v_scale = off;
   off = round_up(off + H * L.s_pad * sizeof(float), 1024);
+  L.stat = off;
+  off = round_up(off + 6 * H * sizeof(float), 1024);
   L.q_pad = (int)round_up(c->max_queries, 4);
   L.q_codes = off;
   off = round_up(off + (size_t)c->max_queries * H * D, 1024);
@@ -249,6 +253,8 @@ int kvring_create(const kvring_config* cfg, void* workspace, size_t workspace_by
   rv.S_pad = L.s_pad;
   rv.n_axes = cfg->n_axes;
   rv.G = cfg->n_global;
+  rv.stat = reinterpret_cast<float*>(ws + L.stat);
+  rv.scale_mode = cfg->scale_mode;
 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   // state, codes and scales (and the query scratch) start at zero: an empty ring
@@ -314,6 +320,7 @@ int kvring_write_global(kvring* r, const void* k, const void* v, const int32_t* 
 
 int kvring_reset_positions(kvring* r, int32_t d, kvring_stream stream) {
   if (!r) return KVRING_ERR_INVALID_ARG;
+  if (r->cfg.scale_mode == KVRING_SCALES_STATIC && !r->calibrated) return KVRING_ERR_SEQUENCE;
   DeltaTable dt{};
   dt.n_pairs = r->cfg.axis_dims[0] / 2;
   for (int j = 0; j < dt.n_pairs; ++j) {
@@ -322,6 +329,17 @@ int kvring_reset_positions(kvring* r, int32_t d, kvring_stream stream) {
   }
   const cudaError_t e = launch_delta_rerotate(r->rv, dt, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? KVRING_OK : cuda_fail(e);
+}
+
+int kvring_calibrate(kvring* r, float margin, kvring_stream stream) {
+  if (!r) return KVRING_ERR_INVALID_ARG;
+  if (!(margin > 0.0f) || !std::isfinite(margin)) return KVRING_ERR_INVALID_ARG;
+  if (r->cfg.scale_mode != KVRING_SCALES_STATIC || r->calibrated || !(r->globals_written || r->window_written))
+    return KVRING_ERR_SEQUENCE;
+  const cudaError_t e = launch_calibrate(r->rv, margin, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  r->calibrated = true;
+  return KVRING_OK;
 }
 
 int kvring_attend(kvring* r, const void* q, const int32_t* q_pos, int32_t n_q, void* out, kvring_stream stream) {
@@ -382,7 +400,8 @@ const char* kvring_status_string(int s) {
     case KVRING_ERR_SCRATCH_LIMIT:
       return "request larger than the static scratch of kvring_attend_noalloc (KVRING_NOALLOC_SCRATCH_BYTES)";
     case KVRING_ERR_SEQUENCE:
-      return "call out of order: the global slots are written once, before the first window write";
+      return "call out of order (global slots: once, before the first window write; fixed scales: "
+             "calibrate once, after a write and before the first reset)";
     default: return "unknown status";
   }
 }

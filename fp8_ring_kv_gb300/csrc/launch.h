@@ -43,6 +43,8 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
 cudaError_t launch_ring_kv_write(const RingView& rv, const void* k, const void* v, const int32_t* pos, int n_new,
                                  bool glob, cudaStream_t st);
 cudaError_t launch_delta_rerotate(const RingView& rv, const DeltaTable& dt, cudaStream_t st);
+// per-head fixed scales from the recorded maxima, then every valid row re-quantised with them
+cudaError_t launch_calibrate(const RingView& rv, float margin, cudaStream_t st);
 cudaError_t launch_debug_quantize(const float* x, long long rows, int d, uint8_t* codes, float* scales,
                                   cudaStream_t st);
 cudaError_t launch_q_prep(const RingView& rv, const void* q, const int32_t* q_pos, int n_q, cudaStream_t st);

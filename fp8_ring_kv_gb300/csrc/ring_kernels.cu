@@ -45,6 +45,11 @@ __device__ __forceinline__ unsigned row_group_mask() {
 // Window write: token i goes to slot G + (wp + i) mod W; then wp <- (wp + N)
 // mod W and n_valid <- min(n_valid + N, S).  Global write (``glob``, the G
 // global tokens, once): token i goes to slot i; then n_valid <- N.
+//
+// Scales: per (token, head) absmax; on a ring with per-head fixed scales
+// (scale_mode 1) the same until calibration, with each row's maximum also
+// folded into its head's recorded maximum, and after it the head's fixed
+// (scale, inv), values beyond the range saturating.
 template <int L>
 __global__ void __launch_bounds__(512, 2) ring_kv_write_kernel(RingView rv, const uint4* __restrict__ k,
                                                                const uint4* __restrict__ v,
@@ -80,9 +85,14 @@ __global__ void __launch_bounds__(512, 2) ring_kv_write_kernel(RingView rv, cons
   }
   if (bad) atomicOr(&rv.state[ST_ERR], DEVERR_POS_RANGE);
 
-  if (threadIdx.x == 0) wp_s = rv.state[ST_WP];
+  __shared__ int fixed_s;
+  if (threadIdx.x == 0) {
+    wp_s = rv.state[ST_WP];
+    fixed_s = rv.scale_mode ? rv.state[ST_STATIC] : 0;
+  }
   __syncthreads();
   const int wp = wp_s;
+  const bool fixed = fixed_s != 0;
   const int W = rv.S - rv.G;
   if (threadIdx.x == 0) {
     const int done = atomicAdd(&rv.state[ST_DONE], 1);
@@ -113,6 +123,12 @@ __global__ void __launch_bounds__(512, 2) ring_kv_write_kernel(RingView rv, cons
     amax = row_max<L>(amax, gm);
     float scale, inv;
     absmax_scale(amax, scale, inv);
+    if (fixed) {
+      scale = rv.stat[STAT_K_SCALE * rv.H + h];
+      inv = rv.stat[STAT_K_INV * rv.H + h];
+    } else if (rv.scale_mode && lane == 0) {
+      atomicMax(reinterpret_cast<int*>(rv.stat) + STAT_AMAX_K * rv.H + h, __float_as_int(amax));
+    }
     *reinterpret_cast<uint4*>(rv.k_codes + row * D + lane * 16) = quant16(x, inv);
     if (lane == 0) rv.k_scale[(size_t)h * rv.S_pad + slot] = scale;
   }
@@ -126,6 +142,12 @@ __global__ void __launch_bounds__(512, 2) ring_kv_write_kernel(RingView rv, cons
     amax = row_max<L>(amax, gm);
     float scale, inv;
     absmax_scale(amax, scale, inv);
+    if (fixed) {
+      scale = rv.stat[STAT_V_SCALE * rv.H + h];
+      inv = rv.stat[STAT_V_INV * rv.H + h];
+    } else if (rv.scale_mode && lane == 0) {
+      atomicMax(reinterpret_cast<int*>(rv.stat) + STAT_AMAX_V * rv.H + h, __float_as_int(amax));
+    }
     *reinterpret_cast<uint4*>(rv.v_codes + row * D + lane * 16) = quant16(x, inv);
     if (lane == 0) rv.v_scale[(size_t)h * rv.S_pad + slot] = scale;
   }
@@ -177,14 +199,16 @@ __global__ void __launch_bounds__(512, 2) q_prep_kernel(RingView rv, const uint4
 
 // ---------------------------------------------------------------- delta_rerotate
 // In place over the window's key rows (head, slot), G <= slot < n_valid
-// (the global keys keep their positions): dequantise
+// (the global keys keep their positions), on a calibrated ring with per-head
+// fixed scales re-quantised with the head's scale (saturating: the clamp)
+// instead of a fresh one: dequantise
 // (code * scale, fp32), rotate the temporal pairs by the host-computed
 // (cos, sin) of -d * omega_j, re-quantise with a fresh absmax scale.  A row
 // is L lanes of 16 codes; the grid is sized to stay resident and each thread
 // walks rows with a stride of the whole grid, loading its next 16 codes and
 // scale before working on the current ones so that two loads are in flight.
 template <int L>
-__global__ void __launch_bounds__(256) delta_rerotate_kernel(RingView rv, DeltaTable dt) {
+__global__ void __launch_bounds__(256, 4) delta_rerotate_kernel(RingView rv, DeltaTable dt) {
   constexpr int D = L * 16;
   // the lanes of a warp read 8 different pairs at once: from shared memory,
   // not from the parameter space (which would serialise them)
@@ -196,6 +220,7 @@ __global__ void __launch_bounds__(256) delta_rerotate_kernel(RingView rv, DeltaT
   // rows are walked as (h, s) over the n_win valid window slots, s = slot - G
   const int n_win = rv.state[ST_NVALID] - rv.G;
   if (n_win <= 0) return;
+  const bool fixed = rv.scale_mode && rv.state[ST_STATIC];
   const int chunks = rv.H * n_win * L;            // <= 128 heads x 2^20 slots x 8
   const int stride = gridDim.x * blockDim.x;      // a multiple of 32: rows never split
   const int lane = threadIdx.x % L;
@@ -246,14 +271,19 @@ __global__ void __launch_bounds__(256) delta_rerotate_kernel(RingView rv, DeltaT
 #pragma unroll
     for (int m = 0; m < 8; ++m)
       if (lane * 8 + m < dt.n_pairs) rope_pair(x[2 * m], x[2 * m + 1], cs[m].x, cs[m].y);
-    float amax = 0.0f;
+    if (fixed) {
+      // the head's scale is kept; values beyond its range saturate
+      *reinterpret_cast<uint4*>(p) = quant16(x, rv.stat[STAT_K_INV * rv.H + h]);
+    } else {
+      float amax = 0.0f;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
-    amax = row_max<L>(amax, __activemask() & row_group_mask<L>());
-    float nscale, inv;
-    absmax_scale(amax, nscale, inv);
-    *reinterpret_cast<uint4*>(p) = quant16(x, inv);
-    if (lane == 0) *sp = nscale;
+      for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
+      amax = row_max<L>(amax, __activemask() & row_group_mask<L>());
+      float nscale, inv;
+      absmax_scale(amax, nscale, inv);
+      *reinterpret_cast<uint4*>(p) = quant16(x, inv);
+      if (lane == 0) *sp = nscale;
+    }
     if (!more) break;
     c = cn;
     h = hn;
@@ -263,6 +293,68 @@ __global__ void __launch_bounds__(256) delta_rerotate_kernel(RingView rv, DeltaT
     code = code_n;
     scale = scale_n;
   }
+}
+
+// ---------------------------------------------------------------- calibration
+// Per-head fixed scales from the recorded maxima (paper §4.3, Appendix G):
+// a = fl32(margin * amax), scale = fl32(a / 448), inv = fl32(448 / a), both
+// 0 when a = 0.  One thread per (tensor, head); marks the ring calibrated.
+__global__ void calib_scales_kernel(RingView rv, float margin) {
+  const int t = threadIdx.x;   // 0 .. 2H-1: K heads, then V heads
+  if (t < 2 * rv.H) {
+    const int v = t >= rv.H;
+    const int h = t - v * rv.H;
+    const float amax = rv.stat[(v ? STAT_AMAX_V : STAT_AMAX_K) * rv.H + h];
+    const float a = __fmul_rn(margin, amax);
+    const float scale = a > 0.0f ? __fdiv_rn(a, kE4m3Max) : 0.0f;
+    const float inv = a > 0.0f ? __fdiv_rn(kE4m3Max, a) : 0.0f;
+    rv.stat[(v ? STAT_V_SCALE : STAT_K_SCALE) * rv.H + h] = scale;
+    rv.stat[(v ? STAT_V_INV : STAT_K_INV) * rv.H + h] = inv;
+  }
+  if (t == 0) rv.state[ST_STATIC] = 1;
+}
+
+// Every valid K and V row, re-quantised with its head's fixed scale from its
+// dequantised value (code * scale, fp32); the row's scale entry becomes the
+// head's.  A row is L lanes of 16 codes; grid-stride over (tensor, head, slot).
+template <int L>
+__global__ void __launch_bounds__(256) calib_requant_kernel(RingView rv) {
+  constexpr int D = L * 16;
+  const int n_valid = rv.state[ST_NVALID];
+  const long long rows = 2LL * rv.H * n_valid;
+  const int lane = threadIdx.x % L;
+  for (long long r = (blockIdx.x * (long long)blockDim.x + threadIdx.x) / L; r < rows;
+       r += (long long)gridDim.x * blockDim.x / L) {
+    const int v = (int)(r / ((long long)rv.H * n_valid));
+    const int rem = (int)(r - (long long)v * rv.H * n_valid);
+    const int h = rem / n_valid;
+    const int slot = rem - h * n_valid;
+    uint8_t* p = (v ? rv.v_codes : rv.k_codes) + ((size_t)h * rv.S + slot) * D + lane * 16;
+    float* sp = (v ? rv.v_scale : rv.k_scale) + (size_t)h * rv.S_pad + slot;
+    const float old = *sp;
+    float x[16];
+    dequant16_codes(*reinterpret_cast<const uint4*>(p), x);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) x[i] = __fmul_rn(x[i], old);
+    *reinterpret_cast<uint4*>(p) = quant16(x, rv.stat[(v ? STAT_V_INV : STAT_K_INV) * rv.H + h]);
+    __syncwarp(row_group_mask<L>());   // every lane has read the old scale before lane 0 replaces it
+    if (lane == 0) *sp = rv.stat[(v ? STAT_V_SCALE : STAT_K_SCALE) * rv.H + h];
+  }
+}
+
+cudaError_t launch_calibrate(const RingView& rv, float margin, cudaStream_t st) {
+  calib_scales_kernel<<<1, 256, 0, st>>>(rv, margin);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int L = rv.D / 16;
+  // enough threads for one pass over a full ring's K and V rows, at most 8 waves of 256-thread blocks
+  long long blocks = (2LL * rv.H * rv.S * L + 255) / 256;
+  if (blocks > 152 * 8) blocks = 152 * 8;
+  if (L == 4)
+    calib_requant_kernel<4><<<(unsigned)blocks, 256, 0, st>>>(rv);
+  else
+    calib_requant_kernel<8><<<(unsigned)blocks, 256, 0, st>>>(rv);
+  return cudaGetLastError();
 }
 
 // ---------------------------------------------------------------- debug quantiser

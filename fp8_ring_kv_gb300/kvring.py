@@ -31,8 +31,12 @@ KVRING_DEVERR_TIMEOUT = 4
 KVRING_OUT_BF16 = 0
 KVRING_OUT_F32 = 1
 
+KVRING_SCALES_TOKEN = 0
+KVRING_SCALES_STATIC = 1
+
 EXPORTS = (
-    "kvring_workspace_bytes", "kvring_create", "kvring_write", "kvring_write_global", "kvring_reset_positions",
+    "kvring_workspace_bytes", "kvring_create", "kvring_write", "kvring_write_global", "kvring_calibrate",
+    "kvring_reset_positions",
     "kvring_attend", "kvring_destroy", "kvring_status_string", "kvring_last_cuda_error",
     "kvring_layout", "kvring_debug_state", "kvring_debug_quantize",
 )
@@ -51,6 +55,7 @@ class kvring_config(ctypes.Structure):
         ("out_dtype", ctypes.c_int32),
         ("max_queries", ctypes.c_int32),
         ("n_global", ctypes.c_int32),
+        ("scale_mode", ctypes.c_int32),
     ]
 
 
@@ -76,6 +81,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "kvring_create": (ctypes.c_int, [cfgp, vp, sz, vp, ctypes.POINTER(vp)]),
         "kvring_write": (ctypes.c_int, [vp, vp, vp, vp, i32, vp]),
         "kvring_write_global": (ctypes.c_int, [vp, vp, vp, vp, i32, vp]),
+        "kvring_calibrate": (ctypes.c_int, [vp, ctypes.c_float, vp]),
         "kvring_reset_positions": (ctypes.c_int, [vp, i32, vp]),
         "kvring_attend": (ctypes.c_int, [vp, vp, vp, i32, vp, vp]),
         "kvring_attend_noalloc": (ctypes.c_int, [vp, vp, vp, i32, vp, vp]),
@@ -115,7 +121,8 @@ def _ptr(t) -> ctypes.c_void_p:
 
 
 def make_config(heads, head_dim, n_slots, axis_dims, pos_min, pos_count, rope_base=10000.0,
-                out_dtype=KVRING_OUT_F32, max_queries=None, n_global=0) -> kvring_config:
+                out_dtype=KVRING_OUT_F32, max_queries=None, n_global=0,
+                scale_mode=KVRING_SCALES_TOKEN) -> kvring_config:
     """max_queries defaults to n_slots (a call attends at most one ring's worth of queries)."""
     c = kvring_config()
     c.heads, c.head_dim, c.n_slots = int(heads), int(head_dim), int(n_slots)
@@ -128,6 +135,7 @@ def make_config(heads, head_dim, n_slots, axis_dims, pos_min, pos_count, rope_ba
     c.out_dtype = int(out_dtype)
     c.max_queries = int(n_slots if max_queries is None else max_queries)
     c.n_global = int(n_global)
+    c.scale_mode = int(scale_mode)
     return c
 
 
@@ -150,6 +158,10 @@ def kvring_write(handle, k, v, pos, n_new: int, stream=None) -> None:
 def kvring_write_global(handle, k, v, pos, n: int, stream=None) -> None:
     check(load().kvring_write_global(handle, _ptr(k), _ptr(v), _ptr(pos), int(n), _stream(stream)),
           "kvring_write_global")
+
+
+def kvring_calibrate(handle, margin: float = 1.5, stream=None) -> None:
+    check(load().kvring_calibrate(handle, float(margin), _stream(stream)), "kvring_calibrate")
 
 
 def kvring_reset_positions(handle, d: int, stream=None) -> None:
@@ -185,9 +197,10 @@ class KVRing:
     the current (or given) stream and return at once."""
 
     def __init__(self, heads, head_dim, n_slots, axis_dims, pos_min, pos_count, rope_base=10000.0,
-                 out_dtype=KVRING_OUT_F32, device="cuda", stream=None, max_queries=None, n_global=0):
+                 out_dtype=KVRING_OUT_F32, device="cuda", stream=None, max_queries=None, n_global=0,
+                 scale_mode=KVRING_SCALES_TOKEN):
         self.cfg = make_config(heads, head_dim, n_slots, axis_dims, pos_min, pos_count, rope_base, out_dtype,
-                               max_queries, n_global)
+                               max_queries, n_global, scale_mode)
         nbytes = kvring_workspace_bytes(self.cfg)
         if nbytes == 0:
             raise KVRingError("invalid kvring configuration")
@@ -215,13 +228,17 @@ class KVRing:
     @classmethod
     def from_shape(cls, shape, out_dtype=KVRING_OUT_F32, device="cuda", stream=None, max_queries=None):
         return cls(shape.heads, shape.head_dim, shape.n_slots, shape.axis_dims, shape.pos_min, shape.pos_count,
-                   shape.rope_base, out_dtype, device, stream, max_queries, getattr(shape, "n_global", 0))
+                   shape.rope_base, out_dtype, device, stream, max_queries, getattr(shape, "n_global", 0),
+                   KVRING_SCALES_STATIC if getattr(shape, "scale_mode", "token") == "static" else KVRING_SCALES_TOKEN)
 
     def write(self, k, v, pos, stream=None):
         kvring_write(self.handle, k, v, pos, k.shape[0], stream)
 
     def write_global(self, k, v, pos, stream=None):
         kvring_write_global(self.handle, k, v, pos, k.shape[0], stream)
+
+    def calibrate(self, margin=1.5, stream=None):
+        kvring_calibrate(self.handle, margin, stream)
 
     def reset_positions(self, d, stream=None):
         kvring_reset_positions(self.handle, d, stream)

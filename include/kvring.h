@@ -60,8 +60,11 @@ enum {
   KVRING_ERR_CUDA = -4,         /* a CUDA runtime/driver call failed; kvring_last_cuda_error says which */
   KVRING_ERR_WORKSPACE = -5,    /* workspace too small */
   KVRING_ERR_NO_DEVICE = -6,    /* no sm_100-family GPU is current */
-  KVRING_ERR_SEQUENCE = -8      /* call out of order (global slots: once, before any window write) */
+  KVRING_ERR_SEQUENCE = -8      /* call out of order (global slots: once, before any window write;
+                                   fixed scales: calibrate once, after a write, before any reset) */
 };
+
+enum { KVRING_SCALES_TOKEN = 0, KVRING_SCALES_STATIC = 1 };
 
 /* bits of the device-side error word */
 enum {
@@ -100,6 +103,13 @@ enum { KVRING_OUT_BF16 = 0, KVRING_OUT_F32 = 1 };
  *              and never rotated; the window ring is slots n_global ..
  *              n_slots-1 (W = n_slots - n_global of them).  0: the whole
  *              cache is the window ring.
+ *   scale_mode KVRING_SCALES_TOKEN: one scale per (token, head) row, its
+ *              absmax / 448, recomputed at write and at reset.
+ *              KVRING_SCALES_STATIC: the paper's per-(cache, head) scales
+ *              (§4.3, App. G): per token until kvring_calibrate, which fixes
+ *              one K and one V scale per head from the maxima written so far
+ *              times a margin; from then on writes use them and resets keep
+ *              them, values beyond the range saturating.
  */
 typedef struct {
   int32_t heads;
@@ -113,6 +123,7 @@ typedef struct {
   int32_t out_dtype;
   int32_t max_queries;
   int32_t n_global;
+  int32_t scale_mode;
 } kvring_config;
 
 /* Bytes of device workspace kvring_create needs for this configuration
@@ -164,6 +175,30 @@ int kvring_write_global(kvring* r, const void* k, const void* v, const int32_t* 
                         kvring_stream stream);
 
 /*
+ * Fix the per-head scales of a KVRING_SCALES_STATIC ring (paper §4.3 and
+ * App. G: scales calibrated once per session from the amax of what the first
+ * steps wrote, times a margin of 1.5).  Until this call the write kernel
+ * quantises per (token, head) and records, per head, the largest |value| of
+ * K (after RoPE) and of V it wrote.  This call, enqueued on ``stream``:
+ *   a = fl32(margin * amax), scale = fl32(a / 448), inv = fl32(448 / a)
+ *   (0 and 0 when a = 0), for K and for V of every head; then every valid
+ *   slot's K and V rows are re-quantised from their dequantised values (code *
+ *   scale, fp32) as e4m3_rn_satfinite(fl32(x * inv)) and their scale entries
+ *   set to the head's scale.
+ * Later writes quantise with these scales (values beyond 448 * scale
+ * saturate) and resets keep them (rotated keys beyond the range saturate:
+ * the paper's clamp).  Attention is unchanged: every slot's scale entry holds
+ * its head's scale.  The ring's mode is read on the device, so a captured
+ * write stays valid across the calibration.
+ *   margin  > 0, finite (else KVRING_ERR_INVALID_ARG); the paper uses 1.5
+ * KVRING_ERR_SEQUENCE, before anything is enqueued, unless the ring is
+ * KVRING_SCALES_STATIC, not yet calibrated, and has been written to; a
+ * kvring_reset_positions on such a ring before its calibration is refused
+ * the same way.
+ */
+int kvring_calibrate(kvring* r, float margin, kvring_stream stream);
+
+/*
  * Position reset by d (delta_rerotate).  Paper §4.2 and App. G: every cached
  * key moves from temporal position p to p - d; with RoPE angles affine in the
  * position, that is one rotation R(-d * omega_{0,j}) of each temporal-axis
@@ -171,8 +206,9 @@ int kvring_write_global(kvring* r, const void* k, const void* v, const int32_t* 
  * keys' positions do not depend on the window) is dequantised (code * scale,
  * fp32), its temporal pairs are rotated in fp32 by the fp32-rounded cos/sin
  * of -d * omega_{0,j} (formed in fp64 on the host), and the row is
- * re-quantised with a fresh absmax scale, in place.  Values and global keys
- * are not touched.  ``d`` is a
+ * re-quantised with a fresh absmax scale (on a calibrated
+ * KVRING_SCALES_STATIC ring: with its head's fixed scale, saturating), in
+ * place.  Values and global keys are not touched.  ``d`` is a
  * host value and is baked into a captured graph.  Callers pass positions
  * shifted by -d to later calls; the library keeps no position counter.
  */

@@ -32,6 +32,11 @@ Workloads (the shapes the paper describes: 757 new tokens per write into a
                  (s mod 7)*757 + i, the window reset by 7*757 before step 7;
                  1% of the channels x8.  ``windowed_tiny``: the same on
                  H=2, D=64, 10 globals, three 16-token frames, 3-axis RoPE.
+7. ``static_scales`` / ``static_scales_tiny``: the windowed workloads (ten
+                 steps, the reset before step 7) on a ring with per-head
+                 fixed scales, calibrated (margin 1.5) on entering the
+                 seventh step; step 8's K and V are scaled x3 so that values
+                 pass the calibrated range.
 """
 from __future__ import annotations
 
@@ -60,6 +65,7 @@ class Shape:
     pos_count: Tuple[int, ...]      #   pos_min .. pos_min + pos_count - 1
     rope_base: float = 10000.0
     n_global: int = 0               # global slots ahead of the window ring
+    scale_mode: str = "token"       # "token" or "static" (per-head scales fixed by a calibration)
 
     @property
     def n_axes(self):
@@ -83,6 +89,12 @@ class WriteGlobal:
 
 
 @dataclass
+class Calibrate:
+    margin: float = 1.5
+    ring: int = 0
+
+
+@dataclass
 class Reset:
     d: int
     ring: int = 0
@@ -101,7 +113,7 @@ class Workload:
     name: str
     shape: Shape
     n_rings: int
-    ops: Iterator           # of WriteGlobal / Write / Reset / Attend
+    ops: Iterator           # of WriteGlobal / Write / Calibrate / Reset / Attend
     note: str = ""
 
 
@@ -363,3 +375,34 @@ def windowed_tiny(steps: int = 8, period: int = 4) -> Workload:
             yield Write(normal_bf16(g, (N, H, D)), normal_bf16(g, (N, H, D)), pos)
             yield Attend(normal_bf16(g, (N, H, D)), pos, tag=f"t{s}")
     return Workload("windowed_tiny", shape, 1, ops())
+
+
+STATIC_MARGIN = 1.5
+CALIBRATION_STEPS = 6
+
+
+def _static(wl: Workload, big_step: int) -> Workload:
+    """``wl`` on a ring with per-head fixed scales: calibrate after the
+    sixth window write; the K and V of write ``big_step`` scaled x3."""
+    shape = Shape(**{**wl.shape.__dict__, "scale_mode": "static"})
+
+    def ops():
+        n_writes = 0
+        for op in wl.ops:
+            if isinstance(op, Write):
+                if n_writes == CALIBRATION_STEPS:
+                    yield Calibrate(STATIC_MARGIN)
+                if n_writes == big_step:
+                    op = Write(op.k * 3, op.v * 3, op.pos, op.ring)   # rounded to bf16; both sides read it
+                n_writes += 1
+            yield op
+    return Workload("static_" + wl.name, shape, wl.n_rings, ops())
+
+
+def static_scales(steps: int = WINDOWED_STEPS) -> Workload:
+    return _static(windowed(steps), big_step=8)
+
+
+def static_scales_tiny() -> Workload:
+    """windowed_tiny over ten steps, reset by 7 before step 7 (after the calibration)."""
+    return _static(windowed_tiny(steps=10, period=7), big_step=8)

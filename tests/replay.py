@@ -78,7 +78,8 @@ def replay(wl: synth.Workload, *, cache_every=1, attend_filter=None, oracle_ring
     sh = wl.shape
     rings = [gpu_ring(sh, out_f32) for _ in range(wl.n_rings)]
     follow = set(range(wl.n_rings)) if oracle_rings is None else set(oracle_rings)
-    refs = {r: OracleRing(sh.heads, sh.head_dim, sh.n_slots, sh.axis_dims, sh.rope_base, n_global=sh.n_global)
+    refs = {r: OracleRing(sh.heads, sh.head_dim, sh.n_slots, sh.axis_dims, sh.rope_base, n_global=sh.n_global,
+                          scale_mode=sh.scale_mode)
             for r in follow}
     rep = Report()
     n_cache = 0
@@ -97,6 +98,12 @@ def replay(wl: synth.Workload, *, cache_every=1, attend_filter=None, oracle_ring
                 n_cache += 1
                 if cache_every and n_cache % cache_every == 0:
                     compare_cache(g, o, f"after write {rep.writes}")
+        elif isinstance(op, synth.Calibrate):
+            g.calibrate(op.margin)
+            if o is not None:
+                o.calibrate(op.margin)
+                assert g.debug_state() == (o.wp, o.n_valid, 0)
+                compare_cache(g, o, "after the calibration")
         elif isinstance(op, synth.Reset):
             g.reset_positions(op.d)
             rep.resets += 1

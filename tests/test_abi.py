@@ -73,13 +73,14 @@ def test_workspace_bytes_valid_configuration(lib):
     # global slots are part of the n_slots, not extra
     assert K.kvring_workspace_bytes(paper_config(n_global=1246)) == n
     assert K.kvring_workspace_bytes(paper_config(n_global=5787)) == n
+    assert K.kvring_workspace_bytes(paper_config(scale_mode=K.KVRING_SCALES_STATIC)) == n
 
 
 @pytest.mark.parametrize("field,value", [
     ("head_dim", 96), ("head_dim", 256), ("heads", 0), ("n_slots", 0), ("n_slots", (1 << 20) + 1),
     ("n_axes", 0), ("n_axes", 4), ("rope_base", 1.0), ("rope_base", math.nan), ("rope_base", math.inf),
     ("out_dtype", 7), ("max_queries", 0), ("max_queries", (1 << 20) + 1),
-    ("n_global", -1), ("n_global", 5788), ("n_global", 6000),
+    ("n_global", -1), ("n_global", 5788), ("n_global", 6000), ("scale_mode", 2), ("scale_mode", -1),
 ])
 def test_workspace_bytes_rejects_invalid(lib, field, value):
     assert K.kvring_workspace_bytes(paper_config(**{field: value})) == 0
@@ -132,6 +133,7 @@ def test_calls_on_null_handle(lib):
     p = _vp(1 << 20)
     assert lib.kvring_write(None, p, p, p, 1, None) == K.KVRING_ERR_INVALID_ARG
     assert lib.kvring_write_global(None, p, p, p, 1, None) == K.KVRING_ERR_INVALID_ARG
+    assert lib.kvring_calibrate(None, 1.5, None) == K.KVRING_ERR_INVALID_ARG
     assert lib.kvring_reset_positions(None, 5, None) == K.KVRING_ERR_INVALID_ARG
     assert lib.kvring_attend(None, p, p, 1, p, None) == K.KVRING_ERR_INVALID_ARG
     assert lib.kvring_attend_noalloc(None, p, p, 1, p, None) == K.KVRING_ERR_INVALID_ARG

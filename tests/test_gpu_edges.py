@@ -192,3 +192,58 @@ def test_reset_before_any_window_write_leaves_the_globals():
     out = ring.attend(q.cuda(), torch.from_numpy(qpos).cuda()).cpu().numpy()
     compare_attention(out, o.attend(synth.to_f32(q), qpos), "attend over the globals alone")
     ring.close()
+
+
+def test_calibration_call_rules():
+    K, lib = _lib()
+    sh = synth.Shape(2, 64, 40, (64,), (0,), (256,), scale_mode="static")
+    ring = _ring(sh)
+    dev = torch.device("cuda")
+    k = torch.ones((4, sh.heads, sh.head_dim), dtype=torch.bfloat16, device=dev)
+    pos = torch.zeros((4, 1), dtype=torch.int32, device=dev)
+    h = ring.handle
+    assert lib.kvring_calibrate(h, 1.5, None) == K.KVRING_ERR_SEQUENCE          # nothing written yet
+    ring.write(k, k, pos)
+    assert lib.kvring_reset_positions(h, 3, None) == K.KVRING_ERR_SEQUENCE      # calibrate first
+    assert lib.kvring_calibrate(h, 0.0, None) == K.KVRING_ERR_INVALID_ARG
+    assert lib.kvring_calibrate(h, float("nan"), None) == K.KVRING_ERR_INVALID_ARG
+    assert lib.kvring_calibrate(h, 1.5, None) == K.KVRING_OK
+    assert lib.kvring_calibrate(h, 1.5, None) == K.KVRING_ERR_SEQUENCE          # once
+    assert lib.kvring_reset_positions(h, 3, None) == K.KVRING_OK
+    torch.cuda.synchronize()
+    assert ring.debug_state() == (4, 4, 0)
+    ring.close()
+    plain = _ring(_tiny_shape())
+    plain.write(k, k, pos)
+    assert lib.kvring_calibrate(plain.handle, 1.5, None) == K.KVRING_ERR_SEQUENCE  # per-token scales
+    plain.close()
+
+
+def test_a_captured_write_follows_the_calibration():
+    """The scale mode is read on the device: one captured write, replayed
+    before and after the calibration, quantises per token and then with the
+    fixed scales."""
+    sh = synth.Shape(2, 64, 64, (16, 24, 24), (0, 0, 0), (8, 4, 4), scale_mode="static")
+    ring = _ring(sh)
+    o = OracleRing(sh.heads, sh.head_dim, sh.n_slots, sh.axis_dims, sh.rope_base, scale_mode="static")
+    g = synth.rng(80)
+    k = synth.normal_bf16(g, (12, sh.heads, sh.head_dim))
+    v = synth.normal_bf16(g, (12, sh.heads, sh.head_dim))
+    pos = np.stack([np.arange(12) % 8, np.arange(12) % 4, np.arange(12) // 4 % 4], 1).astype(np.int32)
+    kd, vd, pd = k.cuda(), v.cuda(), torch.from_numpy(pos).cuda()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        ring.write(kd, vd, pd)
+    torch.cuda.synchronize()
+    assert ring.debug_state() == (0, 0, 0)          # captured, not run
+    graph.replay()
+    o.write(synth.to_f32(k), synth.to_f32(v), pos)
+    ring.calibrate(1.5)
+    o.calibrate(1.5)
+    graph.replay()
+    o.write(synth.to_f32(k), synth.to_f32(v), pos)
+    torch.cuda.synchronize()
+    assert ring.debug_state() == (o.wp, o.n_valid, 0)
+    compare_cache(ring, o, "captured write after the calibration")
+    ring.close()

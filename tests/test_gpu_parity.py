@@ -84,3 +84,19 @@ def test_global_slots_at_paper_layout():
     rep = replay(synth.windowed(), attend_filter=lambda t: t in keep)
     assert rep.writes == 11 and rep.resets == 1 and rep.attend_checked == len(keep)
     print("windowed", rep.attend_stats, f"{rep.seconds:.1f}s")
+
+
+def test_static_scales_tiny():
+    """Per-head scales fixed by a calibration on entering the seventh step,
+    a reset after it (clamping), a step whose values pass the range; every
+    call compared."""
+    rep = replay(synth.static_scales_tiny())
+    assert rep.resets == 1 and rep.attend_checked == 10
+    print("static_tiny", rep.attend_stats)
+
+
+def test_static_scales_at_paper_layout():
+    keep = {"s5", "s6", "s7", "s8", "s9"}
+    rep = replay(synth.static_scales(), attend_filter=lambda t: t in keep)
+    assert rep.resets == 1 and rep.attend_checked == len(keep)
+    print("static", rep.attend_stats, f"{rep.seconds:.1f}s")

@@ -180,3 +180,30 @@ def test_static_mode_call_rules():
     with pytest.raises(ValueError):
         ring.calibrate()                            # once per session
     ring.reset_positions(3)
+
+
+def test_static_workloads_replay_on_the_oracle():
+    """The seeded static-scale workloads follow the call rules; the x3 step
+    drives some values past the calibrated range (saturated codes appear)."""
+    import synth
+    wl = synth.static_scales_tiny()
+    sh = wl.shape
+    ring = OracleRing(sh.heads, sh.head_dim, sh.n_slots, sh.axis_dims, sh.rope_base, n_global=sh.n_global,
+                      scale_mode=sh.scale_mode)
+    kinds = []
+    for op in wl.ops:
+        kinds.append(type(op).__name__)
+        if isinstance(op, synth.WriteGlobal):
+            ring.write_global(synth.to_f32(op.k), synth.to_f32(op.v), op.pos)
+        elif isinstance(op, synth.Write):
+            ring.write(synth.to_f32(op.k), synth.to_f32(op.v), op.pos)
+        elif isinstance(op, synth.Calibrate):
+            ring.calibrate(op.margin)
+        elif isinstance(op, synth.Reset):
+            ring.reset_positions(op.d)
+        else:
+            assert np.all(np.isfinite(ring.attend(synth.to_f32(op.q), op.pos)))
+    assert kinds.count("Calibrate") == 1 and kinds.count("Reset") == 1
+    assert kinds.index("Calibrate") < kinds.index("Reset")
+    vals = np.abs(e4m3.decode(np.concatenate([ring.k_codes, ring.v_codes])))
+    assert (vals == 448.0).any()

@@ -35,8 +35,8 @@ Workloads (the shapes the paper describes: 757 new tokens per write into a
 7. ``static_scales`` / ``static_scales_tiny``: the windowed workloads (ten
                  steps, the reset before step 7) on a ring with per-head
                  fixed scales, calibrated (margin 1.5) on entering the
-                 seventh step; step 8's K and V are scaled x3 so that values
-                 pass the calibrated range.
+                 seventh step; in the tiny one step 8's K and V are scaled x3
+                 so that values pass the calibrated range.
 """
 from __future__ import annotations
 
@@ -381,9 +381,9 @@ STATIC_MARGIN = 1.5
 CALIBRATION_STEPS = 6
 
 
-def _static(wl: Workload, big_step: int) -> Workload:
+def _static(wl: Workload, big_step=None) -> Workload:
     """``wl`` on a ring with per-head fixed scales: calibrate after the
-    sixth window write; the K and V of write ``big_step`` scaled x3."""
+    sixth window write; the K and V of write ``big_step`` (if any) scaled x3."""
     shape = Shape(**{**wl.shape.__dict__, "scale_mode": "static"})
 
     def ops():
@@ -400,7 +400,8 @@ def _static(wl: Workload, big_step: int) -> Workload:
 
 
 def static_scales(steps: int = WINDOWED_STEPS) -> Workload:
-    return _static(windowed(steps), big_step=8)
+    """The paper's layout and input recipe with the paper's scales."""
+    return _static(windowed(steps))
 
 
 def static_scales_tiny() -> Workload:

@@ -347,9 +347,15 @@ cudaError_t launch_calibrate(const RingView& rv, float margin, cudaStream_t st) 
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int L = rv.D / 16;
-  // enough threads for one pass over a full ring's K and V rows, at most 8 waves of 256-thread blocks
+  // enough threads for one pass over a full ring's K and V rows, at most 8
+  // blocks of 256 per SM (the kernel strides over the rest)
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
+      (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+    return e;
   long long blocks = (2LL * rv.H * rv.S * L + 255) / 256;
-  if (blocks > 152 * 8) blocks = 152 * 8;
+  if (blocks > 8LL * sms) blocks = 8LL * sms;
+  if (blocks < 1) blocks = 1;
   if (L == 4)
     calib_requant_kernel<4><<<(unsigned)blocks, 256, 0, st>>>(rv);
   else

@@ -25,6 +25,8 @@ Every function is written from the plain definition of what it computes:
   or per head fixed by ``calibrate``), and the whole call sequence
   (write_global / write / calibrate / reset_positions / attend).
 * ``attention`` -- dense softmax attention in fp64.
+* ``norm``  -- RMS normalisation of Q and K ahead of RoPE (the fused
+  pre-attention step), each step one fixed rounding.
 
 Parity pins (tests/test_oracle_*.py) tie each function to something other than
 itself: closed forms, invariants, brute force, the library float8 cast of

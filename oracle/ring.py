@@ -31,6 +31,10 @@ ring above.  A ring of six latent frames (Appendix G) is the window ring with
 W = 6 x 757 and writes of 757 tokens: every frame then fills whole,
 consecutive slots and the seventh frame replaces the first.
 
+Fused pre-attention (§4.4; Appendix G): ``write``, ``write_global`` and
+``attend`` take an optional ``norm = (gamma, eps)`` that RMS-normalises K
+(or Q) per head before RoPE (``oracle.norm``); V is not normalised.
+
 Scales (``scale_mode``).  "token" (the default): one scale per (token,
 head), recomputed at write and at reset (absmax, see ``quant``).  "static":
 the paper's own scheme (§4.3 "FP8 at write"; Appendix G) -- until
@@ -45,7 +49,7 @@ resets every 42.
 """
 import numpy as np
 
-from . import quant, rope
+from . import norm, quant, rope
 from .attention import attend_f64
 
 
@@ -78,9 +82,12 @@ class OracleRing:
     def slots_for(self, n_new):
         return self.G + (self.wp + np.arange(n_new)) % self.W
 
-    def _store(self, k, v, pos, slots):
-        """RoPE on K (fp32), e4m3 of K and V (per-token absmax scales, or the
-        fixed per-head ones once calibrated), into ``slots``."""
+    def _store(self, k, v, pos, slots, norm_k=None):
+        """RMS norm of K (if asked), RoPE on K (fp32), e4m3 of K and V
+        (per-token absmax scales, or the fixed per-head ones once
+        calibrated), into ``slots``."""
+        if norm_k is not None:
+            k = norm.rms_norm_bf16(k, norm_k[0], norm_k[1])
         kr = rope.rope_f32(k, pos, self.axis_dims, self.base)
         if self.static is None:
             kc, ks = quant.quantize_rows(kr)
@@ -100,7 +107,7 @@ class OracleRing:
         self.k_scale[:, slots] = ks.T
         self.v_scale[:, slots] = vs.T
 
-    def write(self, k, v, pos):
+    def write(self, k, v, pos, norm_k=None):
         """k, v: float32 [N, H, D] (bf16 values); pos: int [N, n_axes].
         Window write.  Returns the slot index of each token."""
         k = np.asarray(k, np.float32)
@@ -111,12 +118,12 @@ class OracleRing:
         if self.G and not self.globals_written:
             raise ValueError("the global slots are written before the first window write")
         slots = self.slots_for(n)
-        self._store(k, v, pos, slots)
+        self._store(k, v, pos, slots, norm_k)
         self.wp = int((self.wp + n) % self.W)
         self.n_valid = int(min(self.n_valid + n, self.S))
         return slots
 
-    def write_global(self, k, v, pos):
+    def write_global(self, k, v, pos, norm_k=None):
         """The G global tokens of the session, once, into slots 0 .. G-1
         (same arithmetic as a window write).  Returns their slots."""
         k = np.asarray(k, np.float32)
@@ -126,7 +133,7 @@ class OracleRing:
         if self.globals_written or self.n_valid:
             raise ValueError("the global slots are written once, before any window write")
         slots = np.arange(self.G)
-        self._store(k, v, pos, slots)
+        self._store(k, v, pos, slots, norm_k)
         self.globals_written = True
         self.n_valid = self.G
         return slots
@@ -171,18 +178,21 @@ class OracleRing:
         self.k_codes[:, lo:hi] = codes
 
     # -- attend --------------------------------------------------------------
-    def quantized_queries(self, q, q_pos):
-        """RoPE (fp32) then per-token-per-head e4m3: (codes [Nq,H,D], scale [Nq,H])."""
-        return quant.quantize_rows(rope.rope_f32(np.asarray(q, np.float32), q_pos,
-                                                 self.axis_dims, self.base))
+    def quantized_queries(self, q, q_pos, norm_q=None):
+        """RMS norm (if asked), RoPE (fp32), then per-token-per-head e4m3:
+        (codes [Nq,H,D], scale [Nq,H])."""
+        q = np.asarray(q, np.float32)
+        if norm_q is not None:
+            q = norm.rms_norm_bf16(q, norm_q[0], norm_q[1])
+        return quant.quantize_rows(rope.rope_f32(q, q_pos, self.axis_dims, self.base))
 
-    def attend(self, q, q_pos, heads=None, rows=None):
+    def attend(self, q, q_pos, heads=None, rows=None, norm_q=None):
         """fp64 attention of the quantised queries over the valid slots.
 
         q: float32 [Nq, H, D] (bf16 values); q_pos: int [Nq, n_axes].
         ``heads`` / ``rows`` restrict the output to some heads / query rows
         (for sampled checks); the result is [len(rows), len(heads), D]."""
-        qc, qs = self.quantized_queries(q, q_pos)
+        qc, qs = self.quantized_queries(q, q_pos, norm_q)
         heads = np.arange(self.H) if heads is None else np.asarray(heads)
         rows = np.arange(qc.shape[0]) if rows is None else np.asarray(rows)
         qh = quant.dequantize_rows_f64(qc[rows][:, heads], qs[rows][:, heads])

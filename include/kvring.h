@@ -20,8 +20,8 @@
  *
  * Memory: the caller owns all device memory.  kvring_create carves one
  * caller-allocated device workspace (kvring_workspace_bytes bytes, 256-byte
- * aligned) into the ring state, the RoPE tables, the e4m3 code arrays and the
- * scale arrays.  The handle itself owns host memory only; kvring_destroy
+ * aligned) into the ring state, the RoPE tables, the e4m3 code arrays, the
+ * scale arrays, a per-head scale table (6 x H fp32) and the query scratch.  The handle itself owns host memory only; kvring_destroy
  * frees that and nothing else.
  *
  * Numbers and layouts:

@@ -38,6 +38,9 @@ struct RingView {
   int32_t G;                      // global slots 0 .. G-1; the window ring is slots G .. S-1
   float* stat;                    // per-head fixed scales [6][H] (STAT_*)
   int32_t scale_mode;             // 0: per (token, head) scales; 1: per head, fixed by calibration
+  const uint4* gamma_k;           // RMS-norm weights of K, bf16 [H][D] (null: no norm)
+  const uint4* gamma_q;           // RMS-norm weights of Q, bf16 [H][D] (null: no norm)
+  float norm_eps;
 };
 
 // ---------------------------------------------------------------- numerics
@@ -102,6 +105,27 @@ __device__ __forceinline__ void bf16x8_to_f32(uint4 u, float* x) {
     x[2 * i + 0] = __uint_as_float(w[i] << 16);
     x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
   }
+}
+
+// RMS norm of one row of D = 16 L channels held as 16 per lane (L lanes of
+// one warp, mask gm), in place: S = sum x^2 in fp64 (exact for bf16 inputs
+// unless a row spans an extreme dynamic range), rounded once to fp32;
+// ms = S / D (exact); rstd = 1/sqrt(ms + eps), correctly rounded; then
+// x = bf16(fl32(fl32(x * rstd) * gamma)).  g: this lane's 16 weights.
+template <int L>
+__device__ __forceinline__ void rms_norm16(float* x, const uint4* g, float eps, unsigned gm) {
+  double s = 0.0;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) s += (double)x[i] * (double)x[i];
+#pragma unroll
+  for (int off = L / 2; off > 0; off >>= 1) s += __shfl_xor_sync(gm, s, off);
+  const float ms = __fmul_rn(__double2float_rn(s), 1.0f / (float)(16 * L));
+  const float rstd = __frsqrt_rn(__fadd_rn(ms, eps));
+  float w[16];
+  bf16x8_to_f32(__ldg(g), w);
+  bf16x8_to_f32(__ldg(g + 1), w + 8);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) x[i] = __bfloat162float(__float2bfloat16_rn(__fmul_rn(__fmul_rn(x[i], rstd), w[i])));
 }
 
 // The axis and in-axis index of RoPE pair p, and its table entry for the

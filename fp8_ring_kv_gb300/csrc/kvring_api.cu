@@ -331,6 +331,16 @@ int kvring_reset_positions(kvring* r, int32_t d, kvring_stream stream) {
   return e == cudaSuccess ? KVRING_OK : cuda_fail(e);
 }
 
+int kvring_set_qk_norm(kvring* r, const void* gamma_q, const void* gamma_k, float eps) {
+  if (!r) return KVRING_ERR_INVALID_ARG;
+  if ((gamma_q || gamma_k) && (!(eps > 0.0f) || !std::isfinite(eps))) return KVRING_ERR_INVALID_ARG;
+  if (!aligned(gamma_q, 16) || !aligned(gamma_k, 16)) return KVRING_ERR_MISALIGNED;
+  r->rv.gamma_q = static_cast<const uint4*>(gamma_q);
+  r->rv.gamma_k = static_cast<const uint4*>(gamma_k);
+  r->rv.norm_eps = eps;
+  return KVRING_OK;
+}
+
 int kvring_calibrate(kvring* r, float margin, kvring_stream stream) {
   if (!r) return KVRING_ERR_INVALID_ARG;
   if (!(margin > 0.0f) || !std::isfinite(margin)) return KVRING_ERR_INVALID_ARG;

@@ -50,7 +50,7 @@ __device__ __forceinline__ unsigned row_group_mask() {
 // (scale_mode 1) the same until calibration, with each row's maximum also
 // folded into its head's recorded maximum, and after it the head's fixed
 // (scale, inv), values beyond the range saturating.
-template <int L>
+template <int L, bool kNorm>
 __global__ void __launch_bounds__(512, 2) ring_kv_write_kernel(RingView rv, const uint4* __restrict__ k,
                                                                const uint4* __restrict__ v,
                                                                const int32_t* __restrict__ pos, int n_new, int T,
@@ -115,6 +115,7 @@ __global__ void __launch_bounds__(512, 2) ring_kv_write_kernel(RingView rv, cons
     float x[16];
     bf16x8_to_f32(ka, x);
     bf16x8_to_f32(kb, x + 8);
+    if constexpr (kNorm) rms_norm16<L>(x, rv.gamma_k + (size_t)h * (D / 8) + lane * 2, rv.norm_eps, gm);
 #pragma unroll
     for (int m = 0; m < 8; ++m) rope_pair(x[2 * m], x[2 * m + 1], cs[m].x, cs[m].y);
     float amax = 0.0f;
@@ -158,8 +159,9 @@ __global__ void __launch_bounds__(512, 2) ring_kv_write_kernel(RingView rv, cons
 // e4m3 with one absmax scale per (query, head), into the workspace's query
 // scratch (codes [n_q][H][D], scales [H][Q_pad]) that the attention kernel
 // then loads by TMA.  Same thread layout (T queries x H heads x L lanes per
-// block) and arithmetic as the K side of ring_kv_write.
-template <int L>
+// block) and arithmetic as the K side of ring_kv_write (with the RMS norm of
+// Q first when the ring has Q norm weights).
+template <int L, bool kNorm>
 __global__ void __launch_bounds__(512, 2) q_prep_kernel(RingView rv, const uint4* __restrict__ q,
                                                         const int32_t* __restrict__ pos, int n_q, int T) {
   constexpr int D = L * 16;
@@ -185,6 +187,7 @@ __global__ void __launch_bounds__(512, 2) q_prep_kernel(RingView rv, const uint4
   float x[16];
   bf16x8_to_f32(a, x);
   bf16x8_to_f32(b, x + 8);
+  if constexpr (kNorm) rms_norm16<L>(x, rv.gamma_q + (size_t)h * (D / 8) + lane * 2, rv.norm_eps, row_group_mask<L>());
 #pragma unroll
   for (int m = 0; m < 8; ++m) rope_pair(x[2 * m], x[2 * m + 1], cs[m].x, cs[m].y);
   float amax = 0.0f;
@@ -401,8 +404,11 @@ static cudaError_t launch_write_t(const RingView& rv, const void* k, const void*
   if (T < 1) T = 1;
   const int threads = per_tok * T;
   const int blocks = (n_new + T - 1) / T;
-  return launch_pdl(ring_kv_write_kernel<L>, dim3(blocks), dim3(threads), 0, st, rv, static_cast<const uint4*>(k),
-                    static_cast<const uint4*>(v), pos, n_new, T, glob);
+  if (rv.gamma_k)
+    return launch_pdl(ring_kv_write_kernel<L, true>, dim3(blocks), dim3(threads), 0, st, rv,
+                      static_cast<const uint4*>(k), static_cast<const uint4*>(v), pos, n_new, T, glob);
+  return launch_pdl(ring_kv_write_kernel<L, false>, dim3(blocks), dim3(threads), 0, st, rv,
+                    static_cast<const uint4*>(k), static_cast<const uint4*>(v), pos, n_new, T, glob);
 }
 
 cudaError_t launch_ring_kv_write(const RingView& rv, const void* k, const void* v, const int32_t* pos, int n_new,
@@ -417,11 +423,12 @@ cudaError_t launch_q_prep(const RingView& rv, const void* q, const int32_t* q_po
   int T = 192 / per_q;
   if (T < 1) T = 1;
   const int blocks = (n_q + T - 1) / T;
+  const uint4* qq = static_cast<const uint4*>(q);
   if (L == 4)
-    return launch_pdl(q_prep_kernel<4>, dim3(blocks), dim3(per_q * T), 0, st, rv, static_cast<const uint4*>(q),
-                      q_pos, n_q, T);
-  return launch_pdl(q_prep_kernel<8>, dim3(blocks), dim3(per_q * T), 0, st, rv, static_cast<const uint4*>(q), q_pos,
-                    n_q, T);
+    return rv.gamma_q ? launch_pdl(q_prep_kernel<4, true>, dim3(blocks), dim3(per_q * T), 0, st, rv, qq, q_pos, n_q, T)
+                      : launch_pdl(q_prep_kernel<4, false>, dim3(blocks), dim3(per_q * T), 0, st, rv, qq, q_pos, n_q, T);
+  return rv.gamma_q ? launch_pdl(q_prep_kernel<8, true>, dim3(blocks), dim3(per_q * T), 0, st, rv, qq, q_pos, n_q, T)
+                    : launch_pdl(q_prep_kernel<8, false>, dim3(blocks), dim3(per_q * T), 0, st, rv, qq, q_pos, n_q, T);
 }
 
 // Blocks that stay resident on every SM at once (computed once per process).

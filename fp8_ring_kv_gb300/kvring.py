@@ -36,6 +36,7 @@ KVRING_SCALES_STATIC = 1
 
 EXPORTS = (
     "kvring_workspace_bytes", "kvring_create", "kvring_write", "kvring_write_global", "kvring_calibrate",
+    "kvring_set_qk_norm",
     "kvring_reset_positions",
     "kvring_attend", "kvring_destroy", "kvring_status_string", "kvring_last_cuda_error",
     "kvring_layout", "kvring_debug_state", "kvring_debug_quantize",
@@ -82,6 +83,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "kvring_write": (ctypes.c_int, [vp, vp, vp, vp, i32, vp]),
         "kvring_write_global": (ctypes.c_int, [vp, vp, vp, vp, i32, vp]),
         "kvring_calibrate": (ctypes.c_int, [vp, ctypes.c_float, vp]),
+        "kvring_set_qk_norm": (ctypes.c_int, [vp, vp, vp, ctypes.c_float]),
         "kvring_reset_positions": (ctypes.c_int, [vp, i32, vp]),
         "kvring_attend": (ctypes.c_int, [vp, vp, vp, i32, vp, vp]),
         "kvring_attend_noalloc": (ctypes.c_int, [vp, vp, vp, i32, vp, vp]),
@@ -158,6 +160,12 @@ def kvring_write(handle, k, v, pos, n_new: int, stream=None) -> None:
 def kvring_write_global(handle, k, v, pos, n: int, stream=None) -> None:
     check(load().kvring_write_global(handle, _ptr(k), _ptr(v), _ptr(pos), int(n), _stream(stream)),
           "kvring_write_global")
+
+
+def kvring_set_qk_norm(handle, gamma_q=None, gamma_k=None, eps: float = 1e-6) -> None:
+    gq = None if gamma_q is None else _ptr(gamma_q)
+    gk = None if gamma_k is None else _ptr(gamma_k)
+    check(load().kvring_set_qk_norm(handle, gq, gk, float(eps)), "kvring_set_qk_norm")
 
 
 def kvring_calibrate(handle, margin: float = 1.5, stream=None) -> None:
@@ -239,6 +247,11 @@ class KVRing:
 
     def calibrate(self, margin=1.5, stream=None):
         kvring_calibrate(self.handle, margin, stream)
+
+    def set_qk_norm(self, gamma_q=None, gamma_k=None, eps=1e-6):
+        """bf16 [H, D] device weights (None: off); the tensors are kept alive here."""
+        self._norm_weights = (gamma_q, gamma_k)
+        kvring_set_qk_norm(self.handle, gamma_q, gamma_k, eps)
 
     def reset_positions(self, d, stream=None):
         kvring_reset_positions(self.handle, d, stream)

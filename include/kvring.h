@@ -175,6 +175,24 @@ int kvring_write_global(kvring* r, const void* k, const void* v, const int32_t* 
                         kvring_stream stream);
 
 /*
+ * RMS norm of Q and K ahead of RoPE (paper §4.4 "Fused pre-attention" and
+ * App. G: each block RMS-normalises the new tokens' Q and K, squaring in
+ * fp32, before RoPE and the FP8 write).  Host-only: keeps the pointers; every
+ * later kvring_write / kvring_write_global normalises K, and every later
+ * kvring_attend(_noalloc) normalises Q, in the same kernels.
+ *   gamma_q, gamma_k  device bf16 [H][D] weights (16-byte aligned), owned by
+ *                     the caller and kept alive while in use; NULL turns
+ *                     that norm off (both NULL: no norm, the default)
+ *   eps               > 0 and finite when a weight is given
+ * Per (token, head) row x of D channels: S = sum x_d^2 (bf16 squares summed
+ * in fp64, rounded once to fp32), ms = S / D, rstd = 1/sqrt(fl32(ms + eps))
+ * correctly rounded, x_d <- bf16(fl32(fl32(x_d * rstd) * gamma_d)); RoPE and
+ * quantisation then act on x.  V is not normalised.  A captured graph keeps
+ * the weights that were set when it was captured.
+ */
+int kvring_set_qk_norm(kvring* r, const void* gamma_q, const void* gamma_k, float eps);
+
+/*
  * Fix the per-head scales of a KVRING_SCALES_STATIC ring (paper §4.3 and
  * App. G: scales calibrated once per session from the amax of what the first
  * steps wrote, times a margin of 1.5).  Until this call the write kernel

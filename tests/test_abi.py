@@ -134,6 +134,7 @@ def test_calls_on_null_handle(lib):
     assert lib.kvring_write(None, p, p, p, 1, None) == K.KVRING_ERR_INVALID_ARG
     assert lib.kvring_write_global(None, p, p, p, 1, None) == K.KVRING_ERR_INVALID_ARG
     assert lib.kvring_calibrate(None, 1.5, None) == K.KVRING_ERR_INVALID_ARG
+    assert lib.kvring_set_qk_norm(None, None, None, 1e-6) == K.KVRING_ERR_INVALID_ARG
     assert lib.kvring_reset_positions(None, 5, None) == K.KVRING_ERR_INVALID_ARG
     assert lib.kvring_attend(None, p, p, 1, p, None) == K.KVRING_ERR_INVALID_ARG
     assert lib.kvring_attend_noalloc(None, p, p, 1, p, None) == K.KVRING_ERR_INVALID_ARG

@@ -151,3 +151,18 @@ def test_debug_quantize_host_checks(lib):
     assert lib.kvring_debug_quantize(p, 4, 48, p, p, None) == K.KVRING_ERR_UNSUPPORTED
     assert lib.kvring_debug_quantize(_vp((1 << 20) + 4), 4, 128, p, p, None) == K.KVRING_ERR_MISALIGNED
     assert lib.kvring_debug_quantize(p, 4, 128, p, _vp((1 << 20) + 2), None) == K.KVRING_ERR_MISALIGNED
+
+
+def test_binding_constants_match_the_header():
+    """Every KVRING_* constant the header defines has the same value in the binding."""
+    text = open(HEADERS[0]).read()
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    found = {}
+    for body in re.findall(r"enum\s*\{(.*?)\}", text, flags=re.S):
+        for name, value in re.findall(r"(KVRING_[A-Z0-9_]+)\s*=\s*(-?\d+)", body):
+            found[name] = int(value)
+    m = re.search(r"#define\s+KVRING_NOALLOC_SCRATCH_BYTES\s+\((\d+)u\s*<<\s*(\d+)\)", text)
+    found["KVRING_NOALLOC_SCRATCH_BYTES"] = int(m.group(1)) << int(m.group(2))
+    assert len(found) >= 18
+    for name, value in found.items():
+        assert getattr(K, name) == value, name

@@ -41,7 +41,24 @@ struct RingView {
   const uint4* gamma_k;           // RMS-norm weights of K, bf16 [H][D] (null: no norm)
   const uint4* gamma_q;           // RMS-norm weights of Q, bf16 [H][D] (null: no norm)
   float norm_eps;
+  float* head_stat;               // query scratch: fp32 [H][2] per call: (c, floor) of the attention, below
 };
+
+// ---------------------------------------------------------------- attention range factors
+// The attention stores weights P = e * w * 2^c in fp16 with e <= 2^kAttnLazyLog2
+// and w = max(s_v, floor) per slot; per head, from the largest V scale m over
+// the valid slots: c = 14 - kAttnLazyLog2 - floor(log2 m) (0 if m = 0, clamped
+// to [-64, 64]) keeps every P below 2^15, and floor = 2^-kAttnFloorLog2 *
+// max(m, 2^-c) keeps 2^-c / w <= 2^kAttnFloorLog2 inside fp16.
+constexpr int kAttnLazyLog2 = 10;
+constexpr int kAttnFloorLog2 = 15;
+
+__device__ __forceinline__ void attn_head_factors(float max_sv, float& c, float& floor) {
+  int ci = max_sv > 0.0f ? 14 - kAttnLazyLog2 - ilogbf(max_sv) : 0;
+  ci = ci < -64 ? -64 : (ci > 64 ? 64 : ci);
+  c = (float)ci;
+  floor = ldexpf(fmaxf(max_sv, ldexpf(1.0f, -ci)), -kAttnFloorLog2);
+}
 
 // ---------------------------------------------------------------- numerics
 // These are the exact fp32 operation sequences the method fixes; the compiler

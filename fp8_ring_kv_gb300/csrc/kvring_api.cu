@@ -48,7 +48,7 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct Layout {
-  size_t state, rope[3], k_codes, v_codes, k_scale, v_scale, stat, q_codes, q_scale, total;
+  size_t state, rope[3], k_codes, v_codes, k_scale, v_scale, stat, q_codes, q_scale, head_stat, total;
   int s_pad, q_pad;
 };
 
@@ -99,6 +99,8 @@ Layout layout_of(const kvring_config* c) {
   off = round_up(off + (size_t)c->max_queries * H * D, 1024);
   L.q_scale = off;
   off = round_up(off + H * L.q_pad * sizeof(float), 1024);
+  L.head_stat = off;
+  off = round_up(off + 2 * H * sizeof(float), 1024);
   L.total = off;
   return L;
 }
@@ -246,6 +248,7 @@ int kvring_create(const kvring_config* cfg, void* workspace, size_t workspace_by
   rv.v_scale = reinterpret_cast<float*>(ws + L.v_scale);
   rv.q_codes = ws + L.q_codes;
   rv.q_scale = reinterpret_cast<float*>(ws + L.q_scale);
+  rv.head_stat = reinterpret_cast<float*>(ws + L.head_stat);
   rv.Q_pad = L.q_pad;
   rv.H = cfg->heads;
   rv.D = cfg->head_dim;
@@ -368,11 +371,13 @@ int kvring_attend_noalloc(kvring* r, const void* q, const int32_t* q_pos, int32_
   if (!r || !q || !q_pos || !out) return KVRING_ERR_INVALID_ARG;
   if (n_q < 1) return KVRING_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(out, 16) || !aligned(q_pos, 4)) return KVRING_ERR_MISALIGNED;
-  // scratch layout: e4m3 codes [n_q][H][D], then fp32 scales [H][round_up(n_q, 4)]
+  // scratch layout: e4m3 codes [n_q][H][D], then fp32 scales [H][round_up(n_q, 4)],
+  // then the per-head attention range factors fp32 [H][2]
   const size_t H = r->rv.H, D = r->rv.D;
   const size_t q_pad = round_up((size_t)n_q, 4);
   const size_t scale_off = round_up((size_t)n_q * H * D, 1024);
-  if (scale_off + H * q_pad * sizeof(float) > (size_t)KVRING_NOALLOC_SCRATCH_BYTES) return KVRING_ERR_SCRATCH_LIMIT;
+  const size_t stat_off = scale_off + H * q_pad * sizeof(float);
+  if (stat_off + 2 * H * sizeof(float) > (size_t)KVRING_NOALLOC_SCRATCH_BYTES) return KVRING_ERR_SCRATCH_LIMIT;
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e);
@@ -383,6 +388,7 @@ int kvring_attend_noalloc(kvring* r, const void* q, const int32_t* q_pos, int32_
   RingView rv = r->rv;
   rv.q_codes = scratch;
   rv.q_scale = reinterpret_cast<float*>(scratch + scale_off);
+  rv.head_stat = reinterpret_cast<float*>(scratch + stat_off);
   rv.Q_pad = (int)q_pad;
   CUtensorMap q_map;
   if (!encode_query_map(&q_map, scratch, rv.H, rv.D, n_q)) return cuda_fail(cudaErrorInvalidValue);

@@ -161,18 +161,53 @@ __global__ void __launch_bounds__(512, 2) ring_kv_write_kernel(RingView rv, cons
 // then loads by TMA.  Same thread layout (T queries x H heads x L lanes per
 // block) and arithmetic as the K side of ring_kv_write (with the RMS norm of
 // Q first when the ring has Q norm weights).
+//
+// Blocks past the queries' (one per head, blockIdx.x = n_qblocks + h) find
+// the head's largest V scale over the valid slots and store the attention's
+// per-head range factor and scale floor (attn_head_factors) in the scratch.
 template <int L, bool kNorm>
 __global__ void __launch_bounds__(512, 2) q_prep_kernel(RingView rv, const uint4* __restrict__ q,
-                                                        const int32_t* __restrict__ pos, int n_q, int T) {
+                                                        const int32_t* __restrict__ pos, int n_q, int T,
+                                                        int n_qblocks) {
   constexpr int D = L * 16;
+  pdl_wait();
+  pdl_trigger();
+  if ((int)blockIdx.x >= n_qblocks) {
+    __shared__ float wmax[16];
+    const int h = blockIdx.x - n_qblocks;
+    const int n_valid = rv.state[ST_NVALID];
+    // each head's scale row starts 16-byte aligned (rows are S_pad, a
+    // multiple of 4, apart)
+    const float* vs1 = rv.v_scale + (size_t)h * rv.S_pad;
+    const float4* vs = reinterpret_cast<const float4*>(vs1);
+    const int n4 = n_valid >> 2;
+    float mx = 0.0f;
+#pragma unroll 4
+    for (int i = threadIdx.x; i < n4; i += blockDim.x) {
+      const float4 v = __ldg(vs + i);
+      mx = fmaxf(mx, fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
+    }
+    if ((int)threadIdx.x < (n_valid & 3)) mx = fmaxf(mx, vs1[n4 * 4 + threadIdx.x]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
+    const int nw = (blockDim.x + 31) >> 5;
+    if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = mx;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      for (int w = 1; w < nw; ++w) mx = fmaxf(mx, wmax[w]);
+      float c, fl;
+      attn_head_factors(mx, c, fl);
+      rv.head_stat[2 * h] = c;
+      rv.head_stat[2 * h + 1] = fl;
+    }
+    return;
+  }
   const int per_q = rv.H * L;
   const int tl = threadIdx.x / per_q;
   const int rem = threadIdx.x - tl * per_q;
   const int h = rem / L;
   const int lane = rem % L;
   const int qi = blockIdx.x * T + tl;
-  pdl_wait();
-  pdl_trigger();
   if (qi >= n_q) return;   // whole rows
   const size_t row = (size_t)qi * rv.H + h;
   const uint4* src = q + row * (D / 8) + lane * 2;
@@ -281,7 +316,7 @@ __global__ void __launch_bounds__(256, 4) delta_rerotate_kernel(RingView rv, Del
       float amax = 0.0f;
 #pragma unroll
       for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
-      amax = row_max<L>(amax, __activemask() & row_group_mask<L>());
+      amax = row_max<L>(amax, row_group_mask<L>());
       float nscale, inv;
       absmax_scale(amax, nscale, inv);
       *reinterpret_cast<uint4*>(p) = quant16(x, inv);
@@ -388,7 +423,7 @@ __global__ void __launch_bounds__(256) debug_quantize_kernel(const float* __rest
   float amax = 0.0f;
 #pragma unroll
   for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
-  amax = row_max<L>(amax, __activemask() & row_group_mask<L>());
+  amax = row_max<L>(amax, row_group_mask<L>());
   float scale, inv;
   absmax_scale(amax, scale, inv);
   *reinterpret_cast<uint4*>(codes + row * D + lane * 16) = quant16(v, inv);
@@ -422,13 +457,14 @@ cudaError_t launch_q_prep(const RingView& rv, const void* q, const int32_t* q_po
   const int per_q = rv.H * L;
   int T = 192 / per_q;
   if (T < 1) T = 1;
-  const int blocks = (n_q + T - 1) / T;
+  const int qblocks = (n_q + T - 1) / T;
+  const dim3 grid(qblocks + rv.H), block(per_q * T);   // then one block per head: the range factors
   const uint4* qq = static_cast<const uint4*>(q);
   if (L == 4)
-    return rv.gamma_q ? launch_pdl(q_prep_kernel<4, true>, dim3(blocks), dim3(per_q * T), 0, st, rv, qq, q_pos, n_q, T)
-                      : launch_pdl(q_prep_kernel<4, false>, dim3(blocks), dim3(per_q * T), 0, st, rv, qq, q_pos, n_q, T);
-  return rv.gamma_q ? launch_pdl(q_prep_kernel<8, true>, dim3(blocks), dim3(per_q * T), 0, st, rv, qq, q_pos, n_q, T)
-                    : launch_pdl(q_prep_kernel<8, false>, dim3(blocks), dim3(per_q * T), 0, st, rv, qq, q_pos, n_q, T);
+    return rv.gamma_q ? launch_pdl(q_prep_kernel<4, true>, grid, block, 0, st, rv, qq, q_pos, n_q, T, qblocks)
+                      : launch_pdl(q_prep_kernel<4, false>, grid, block, 0, st, rv, qq, q_pos, n_q, T, qblocks);
+  return rv.gamma_q ? launch_pdl(q_prep_kernel<8, true>, grid, block, 0, st, rv, qq, q_pos, n_q, T, qblocks)
+                    : launch_pdl(q_prep_kernel<8, false>, grid, block, 0, st, rv, qq, q_pos, n_q, T, qblocks);
 }
 
 // Blocks that stay resident on every SM at once (computed once per process).

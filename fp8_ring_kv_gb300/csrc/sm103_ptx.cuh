@@ -80,12 +80,29 @@ __device__ __forceinline__ bool mbar_try_wait_parked(uint64_t* bar, uint32_t par
   return ok != 0;
 }
 
+// Non-blocking test of the phase (never suspends the thread): for a waiter
+// that polls several barriers in turn.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait for the phase with the given parity to complete.  Returns false (and
-// stops waiting) once ``*abort`` becomes non-zero or the time limit passes;
-// in the latter case it raises ``*abort`` itself so every other role of the
-// block stops waiting too.  kParked: see mbar_try_wait_parked.
+// stops waiting) once ``*abort`` becomes non-zero or ``limit_ns`` passes; in
+// the latter case it raises ``*abort`` itself so every other role of the
+// block stops waiting too.  ``abort`` may be null (a wait that only the time
+// limit ends, for draining copies after an abort).  kParked: see
+// mbar_try_wait_parked.
 template <bool kParked = false>
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                          unsigned long long limit_ns = kWaitLimitNs) {
   auto probe = [&]() { return kParked ? mbar_try_wait_parked(bar, parity) : mbar_try_wait(bar, parity); };
   if (probe()) return true;
   const unsigned long long t0 = globaltimer_ns();
@@ -93,6 +110,25 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   while (true) {
     if (probe()) return true;
     if ((++spins & 7u) == 0) {
+      if (abort && *abort) return false;
+      if (globaltimer_ns() - t0 > limit_ns) {
+        if (abort) *abort = 1;
+        return false;
+      }
+    }
+  }
+}
+
+// The same as mbar_wait, polling with the non-blocking test (the thread is
+// never suspended): for waits on the critical path, where a suspended
+// thread's late wake-up would cost more than the issue slots of the poll.
+__device__ __forceinline__ bool mbar_wait_spin(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  if (mbar_test_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer_ns();
+  uint32_t spins = 0;
+  while (true) {
+    if (mbar_test_wait(bar, parity)) return true;
+    if ((++spins & 15u) == 0) {
       if (*abort) return false;
       if (globaltimer_ns() - t0 > kWaitLimitNs) {
         *abort = 1;
@@ -100,6 +136,18 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
       }
     }
   }
+}
+
+__device__ __forceinline__ bool warp_wait_spin(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  return __all_sync(0xFFFFFFFFu, mbar_wait_spin(bar, parity, abort));
+}
+
+// mbar_wait by every lane of a warp, with one answer for all of them (a lane
+// that timed out while another saw the phase complete must not leave the warp
+// divergent at a later warp-collective instruction).
+template <bool kParked = false>
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  return __all_sync(0xFFFFFFFFu, mbar_wait<kParked>(bar, parity, abort));
 }
 
 // ---------------------------------------------------------------- dependent launch
@@ -266,6 +314,35 @@ __device__ __forceinline__ void tmem_st_16x256b_x4(uint32_t taddr, const uint32_
       : "memory");
 }
 
+// 16x256b.x1 (8 columns) load and store, each with its wait.
+__device__ __forceinline__ void tmem_ld_16x256b_x1(uint32_t taddr, uint32_t (&r)[4]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x1.b32 {%0,%1,%2,%3}, [%4];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st_16x256b_x1(uint32_t taddr, const uint32_t (&r)[4]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.16x256b.x1.b32 [%0], {%1,%2,%3,%4};\n\t"
+      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3])
+      : "memory");
+}
+
+// Two 16x256b.x1 loads (lane bases a0 and a1, 8 columns each) and the wait:
+// r[0..3] from a0, r[4..7] from a1, in the 16x256b register order above.
+__device__ __forceinline__ void tmem_ld2_16x256b_x1(uint32_t a0, uint32_t a1, uint32_t (&r)[8]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x1.b32 {%0,%1,%2,%3}, [%8];\n\t"
+      "tcgen05.ld.sync.aligned.16x256b.x1.b32 {%4,%5,%6,%7}, [%9];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+      : "r"(a0), "r"(a1)
+      : "memory");
+}
+
 // 16x128b shape, repetition k (4 columns from col): register 2k holds lane
 // (base + t/4) column 4k + t%4, register 2k + 1 lane (base + t/4 + 8).
 __device__ __forceinline__ void tmem_st_16x128b_x16(uint32_t taddr, const uint32_t (&r)[32]) {
@@ -335,32 +412,12 @@ __device__ __forceinline__ uint32_t cvt_f16x2(float lo, float hi) {
 }
 
 // ---------------------------------------------------------------- packed fp32 pairs
-__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
-  float2 r;
-  asm("{\n\t.reg .b64 a, b, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
-      "mul.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
-      : "=f"(r.x), "=f"(r.y)
-      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-  return r;
-}
-
-__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
-  float2 r;
-  asm("{\n\t.reg .b64 a, b, c, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\tmov.b64 c, {%6, %7};\n\t"
-      "fma.rn.f32x2 d, a, b, c;\n\tmov.b64 {%0, %1}, d;\n\t}"
-      : "=f"(r.x), "=f"(r.y)
-      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
-  return r;
-}
-
-__device__ __forceinline__ float2 add2(float2 a, float2 b) {
-  float2 r;
-  asm("{\n\t.reg .b64 a, b, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
-      "add.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
-      : "=f"(r.x), "=f"(r.y)
-      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-  return r;
-}
+// One FMUL2 / FFMA2 / FADD2 for two fp32 values, each element rounded to
+// nearest even on its own (the compiler's own packed intrinsics, so that it
+// can keep the operands in register pairs without moves).
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+__device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
 
 __device__ __forceinline__ float max3f(float a, float b, float c) {
   float r;

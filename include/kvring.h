@@ -266,10 +266,11 @@ int kvring_attend(kvring* r, const void* q, const int32_t* q_pos, int32_t n_q, v
  *
  *   arguments, output and results: as kvring_attend, except that n_q is not
  *   bounded by the ring's max_queries but by the static scratch:
- *     round_up(n_q * H * D, 1024) + H * round_up(n_q, 4) * 4
+ *     round_up(n_q * H * D, 1024) + H * round_up(n_q, 4) * 4 + 8 * H
  *       <= KVRING_NOALLOC_SCRATCH_BYTES (8 MiB)
- *   e.g. up to 2,647 queries at 24 heads x 128.  A larger request returns
- *   KVRING_ERR_SCRATCH_LIMIT before anything is enqueued.
+ *   (the query codes, their scales and two per-head factors of the
+ *   attention), e.g. up to 2,647 queries at 24 heads x 128.  A larger
+ *   request returns KVRING_ERR_SCRATCH_LIMIT before anything is enqueued.
  *
  * The scratch is one array per device for the whole process.  Calls that
  * can overlap in time on one device (two streams, two host threads, two

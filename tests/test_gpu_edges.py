@@ -247,3 +247,29 @@ def test_a_captured_write_follows_the_calibration():
     assert ring.debug_state() == (o.wp, o.n_valid, 0)
     compare_cache(ring, o, "captured write after the calibration")
     ring.close()
+
+
+def test_fewer_queries_than_the_previous_call():
+    """The query scratch keeps the rows of an earlier, larger call; a later
+    call with fewer queries (a partial last query tile) must not be affected
+    by them.  757, then 300, then 5 queries on one ring, each against the
+    oracle."""
+    wl = synth.single()
+    ops = list(wl.ops)
+    sh = wl.shape
+    ring = _ring(sh)
+    o = OracleRing(sh.heads, sh.head_dim, sh.n_slots, sh.axis_dims, sh.rope_base)
+    dev = torch.device("cuda")
+    for op in ops:
+        if isinstance(op, synth.Write):
+            ring.write(op.k.to(dev), op.v.to(dev), torch.from_numpy(op.pos).to(dev))
+            o.write(synth.to_f32(op.k), synth.to_f32(op.v), op.pos)
+    g = synth.rng(81)
+    heads = [0, 7, 23]
+    for n_q in (757, 300, 5):
+        q = synth.normal_bf16(g, (n_q, sh.heads, sh.head_dim))
+        qpos = synth.lin_pos(sh.n_slots, n_q)
+        out = ring.attend(q.to(dev), torch.from_numpy(qpos).to(dev)).cpu().numpy()[:, heads]
+        compare_attention(out, o.attend(synth.to_f32(q), qpos, heads=heads), f"{n_q} queries")
+    assert ring.debug_state()[2] == 0
+    ring.close()

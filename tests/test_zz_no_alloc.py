@@ -78,7 +78,7 @@ def test_noalloc_rejects_requests_beyond_the_static_scratch():
 
     def need(n):
         ru = lambda x, a: (x + a - 1) // a * a  # noqa: E731
-        return ru(n * H * D, 1024) + H * ru(n, 4) * 4
+        return ru(n * H * D, 1024) + H * ru(n, 4) * 4 + 2 * H * 4
 
     n_max = max(n for n in range(1, 8192) if need(n) <= K.KVRING_NOALLOC_SCRATCH_BYTES)
     q, pos = _queries(shape, n_max + 1, 7)

@@ -64,7 +64,8 @@ __device__ __forceinline__ void attn_head_factors(float max_sv, float& c, float&
 // These are the exact fp32 operation sequences the method fixes; the compiler
 // must not contract or reorder them (no fast-math, explicit _rn intrinsics).
 
-// One RoPE pair: (x0 c - x1 s, x0 s + x1 c), every product and sum rounded.
+// One RoPE pair: (x0 c - x1 s, x0 s + x1 c), every product and sum rounded
+// (the _rn intrinsics are never contracted into a fused multiply-add).
 __device__ __forceinline__ void rope_pair(float& x0, float& x1, float c, float s) {
   const float a = __fsub_rn(__fmul_rn(x0, c), __fmul_rn(x1, s));
   const float b = __fadd_rn(__fmul_rn(x0, s), __fmul_rn(x1, c));
@@ -84,14 +85,35 @@ __device__ __forceinline__ void absmax_scale(float amax, float& scale, float& in
   }
 }
 
+// The same scale and inverse for a row of D = 16 L channels held by L lanes
+// (mask gm): each lane makes one of the two divisions -- the row's first
+// lane amax / 448, its second 448 / amax -- and the row shares them.  Bit for
+// bit the values of absmax_scale.
+template <int L>
+__device__ __forceinline__ void row_absmax_scale(float amax, float& scale, float& inv, unsigned gm) {
+  if constexpr (L == 1) {
+    absmax_scale(amax, scale, inv);
+  } else {
+    const int lane = threadIdx.x & 31;
+    const int base = lane & ~(L - 1);
+    const bool first = (lane & (L - 1)) == 0;
+    const float q = amax > 0.0f ? __fdiv_rn(first ? amax : kE4m3Max, first ? kE4m3Max : amax) : 0.0f;
+    scale = __shfl_sync(gm, q, base);
+    inv = __shfl_sync(gm, q, base + 1);
+  }
+}
+
 // 16 values -> 16 e4m3 codes (round to nearest even, saturating) of x * inv.
 // A zero row (inv == 0) gives all-zero codes (+0).
 __device__ __forceinline__ uint4 quant16(const float* x, float inv) {
   uint32_t w[4];
+  const float2 iv = make_float2(inv, inv);
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const uint32_t lo = cvt_e4m3x2(__fmul_rn(x[4 * i + 0], inv), __fmul_rn(x[4 * i + 1], inv));
-    const uint32_t hi = cvt_e4m3x2(__fmul_rn(x[4 * i + 2], inv), __fmul_rn(x[4 * i + 3], inv));
+    const float2 a = __fmul2_rn(make_float2(x[4 * i + 0], x[4 * i + 1]), iv);
+    const float2 b = __fmul2_rn(make_float2(x[4 * i + 2], x[4 * i + 3]), iv);
+    const uint32_t lo = cvt_e4m3x2(a.x, a.y);
+    const uint32_t hi = cvt_e4m3x2(b.x, b.y);
     w[i] = lo | (hi << 16);
   }
   if (inv == 0.0f) w[0] = w[1] = w[2] = w[3] = 0u;
@@ -107,6 +129,23 @@ __device__ __forceinline__ void dequant16_codes(uint4 c, float* x) {
     const uint32_t hi = cvt_e4m3x2_to_f16x2((uint16_t)(w[i] >> 16));
     const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&lo));
     const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&hi));
+    x[4 * i + 0] = a.x;
+    x[4 * i + 1] = a.y;
+    x[4 * i + 2] = b.x;
+    x[4 * i + 3] = b.y;
+  }
+}
+
+// 16 e4m3 codes -> 16 fp32 values code * scale, each product rounded once.
+__device__ __forceinline__ void dequant16_scaled(uint4 c, float scale, float* x) {
+  const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+  const float2 sc = make_float2(scale, scale);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t lo = cvt_e4m3x2_to_f16x2((uint16_t)(w[i] & 0xFFFFu));
+    const uint32_t hi = cvt_e4m3x2_to_f16x2((uint16_t)(w[i] >> 16));
+    const float2 a = __fmul2_rn(__half22float2(*reinterpret_cast<const __half2*>(&lo)), sc);
+    const float2 b = __fmul2_rn(__half22float2(*reinterpret_cast<const __half2*>(&hi)), sc);
     x[4 * i + 0] = a.x;
     x[4 * i + 1] = a.y;
     x[4 * i + 2] = b.x;

@@ -338,6 +338,10 @@ int kvring_set_qk_norm(kvring* r, const void* gamma_q, const void* gamma_k, floa
   if (!r) return KVRING_ERR_INVALID_ARG;
   if ((gamma_q || gamma_k) && (!(eps > 0.0f) || !std::isfinite(eps))) return KVRING_ERR_INVALID_ARG;
   if (!aligned(gamma_q, 16) || !aligned(gamma_k, 16)) return KVRING_ERR_MISALIGNED;
+  // a calibrated ring's fixed K scales were taken from the keys as they were
+  // normalised then: the K norm may no longer change
+  const bool k_changes = gamma_k != static_cast<const void*>(r->rv.gamma_k) || (gamma_k && eps != r->rv.norm_eps);
+  if (r->calibrated && k_changes) return KVRING_ERR_SEQUENCE;
   r->rv.gamma_q = static_cast<const uint4*>(gamma_q);
   r->rv.gamma_k = static_cast<const uint4*>(gamma_k);
   r->rv.norm_eps = eps;
@@ -447,6 +451,13 @@ int kvring_debug_state(const kvring* r, kvring_stream stream, int32_t* out3) {
   out3[1] = w[ST_NVALID];
   out3[2] = w[ST_ERR];
   return KVRING_OK;
+}
+
+int kvring_debug_wait_timeout(int64_t limit_ns, int32_t complete, int64_t* out2, kvring_stream stream) {
+  if (!out2 || limit_ns < 1 || limit_ns > 10000000000ll) return KVRING_ERR_INVALID_ARG;
+  if (!aligned(out2, 8)) return KVRING_ERR_MISALIGNED;
+  const cudaError_t e = launch_debug_wait(limit_ns, complete != 0, out2, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? KVRING_OK : cuda_fail(e);
 }
 
 int kvring_debug_quantize(const float* x, int64_t rows, int32_t d, uint8_t* codes, float* scales,

@@ -45,6 +45,9 @@ cudaError_t launch_ring_kv_write(const RingView& rv, const void* k, const void* 
 cudaError_t launch_delta_rerotate(const RingView& rv, const DeltaTable& dt, cudaStream_t st);
 // per-head fixed scales from the recorded maxima, then every valid row re-quantised with them
 cudaError_t launch_calibrate(const RingView& rv, float margin, cudaStream_t st);
+// one block whose warps wait on a barrier (complete: it is also completed);
+// out2 = {error bits, nanoseconds waited}
+cudaError_t launch_debug_wait(long long limit_ns, bool complete, int64_t* out2, cudaStream_t st);
 cudaError_t launch_debug_quantize(const float* x, long long rows, int d, uint8_t* codes, float* scales,
                                   cudaStream_t st);
 cudaError_t launch_q_prep(const RingView& rv, const void* q, const int32_t* q_pos, int n_q, cudaStream_t st);

@@ -67,6 +67,13 @@ __global__ void __launch_bounds__(512, 2) ring_kv_write_kernel(RingView rv, cons
   const bool live = tok < n_new;   // uniform over the L lanes of a row
   pdl_wait();
   pdl_trigger();
+  // the write position (and mode) first, so that its latency overlaps the
+  // input loads below
+  int wp0 = 0, fixed0 = 0;
+  if (threadIdx.x == 0) {
+    wp0 = rv.state[ST_WP];
+    fixed0 = rv.scale_mode ? rv.state[ST_STATIC] : 0;
+  }
 
   uint4 ka = make_uint4(0, 0, 0, 0), kb = ka, va = ka, vb = ka;
   if (live) {
@@ -87,8 +94,8 @@ __global__ void __launch_bounds__(512, 2) ring_kv_write_kernel(RingView rv, cons
 
   __shared__ int fixed_s;
   if (threadIdx.x == 0) {
-    wp_s = rv.state[ST_WP];
-    fixed_s = rv.scale_mode ? rv.state[ST_STATIC] : 0;
+    wp_s = wp0;
+    fixed_s = fixed0;
   }
   __syncthreads();
   const int wp = wp_s;
@@ -123,7 +130,7 @@ __global__ void __launch_bounds__(512, 2) ring_kv_write_kernel(RingView rv, cons
     for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
     amax = row_max<L>(amax, gm);
     float scale, inv;
-    absmax_scale(amax, scale, inv);
+    row_absmax_scale<L>(amax, scale, inv, gm);
     if (fixed) {
       scale = rv.stat[STAT_K_SCALE * rv.H + h];
       inv = rv.stat[STAT_K_INV * rv.H + h];
@@ -142,7 +149,7 @@ __global__ void __launch_bounds__(512, 2) ring_kv_write_kernel(RingView rv, cons
     for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
     amax = row_max<L>(amax, gm);
     float scale, inv;
-    absmax_scale(amax, scale, inv);
+    row_absmax_scale<L>(amax, scale, inv, gm);
     if (fixed) {
       scale = rv.stat[STAT_V_SCALE * rv.H + h];
       inv = rv.stat[STAT_V_INV * rv.H + h];
@@ -230,7 +237,7 @@ __global__ void __launch_bounds__(512, 2) q_prep_kernel(RingView rv, const uint4
   for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
   amax = row_max<L>(amax, row_group_mask<L>());
   float scale, inv;
-  absmax_scale(amax, scale, inv);
+  row_absmax_scale<L>(amax, scale, inv, row_group_mask<L>());
   *reinterpret_cast<uint4*>(rv.q_codes + row * D + lane * 16) = quant16(x, inv);
   if (lane == 0) rv.q_scale[(size_t)h * rv.Q_pad + qi] = scale;
 }
@@ -303,9 +310,7 @@ __global__ void __launch_bounds__(256, 4) delta_rerotate_kernel(RingView rv, Del
       scale_n = *spn;
     }
     float x[16];
-    dequant16_codes(code, x);
-#pragma unroll
-    for (int i = 0; i < 16; ++i) x[i] = __fmul_rn(x[i], scale);
+    dequant16_scaled(code, scale, x);
 #pragma unroll
     for (int m = 0; m < 8; ++m)
       if (lane * 8 + m < dt.n_pairs) rope_pair(x[2 * m], x[2 * m + 1], cs[m].x, cs[m].y);
@@ -318,7 +323,7 @@ __global__ void __launch_bounds__(256, 4) delta_rerotate_kernel(RingView rv, Del
       for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
       amax = row_max<L>(amax, row_group_mask<L>());
       float nscale, inv;
-      absmax_scale(amax, nscale, inv);
+      row_absmax_scale<L>(amax, nscale, inv, row_group_mask<L>());
       *reinterpret_cast<uint4*>(p) = quant16(x, inv);
       if (lane == 0) *sp = nscale;
     }
@@ -371,9 +376,7 @@ __global__ void __launch_bounds__(256) calib_requant_kernel(RingView rv) {
     float* sp = (v ? rv.v_scale : rv.k_scale) + (size_t)h * rv.S_pad + slot;
     const float old = *sp;
     float x[16];
-    dequant16_codes(*reinterpret_cast<const uint4*>(p), x);
-#pragma unroll
-    for (int i = 0; i < 16; ++i) x[i] = __fmul_rn(x[i], old);
+    dequant16_scaled(*reinterpret_cast<const uint4*>(p), old, x);
     *reinterpret_cast<uint4*>(p) = quant16(x, rv.stat[(v ? STAT_V_INV : STAT_K_INV) * rv.H + h]);
     __syncwarp(row_group_mask<L>());   // every lane has read the old scale before lane 0 replaces it
     if (lane == 0) *sp = rv.stat[(v ? STAT_V_SCALE : STAT_K_SCALE) * rv.H + h];
@@ -401,6 +404,40 @@ cudaError_t launch_calibrate(const RingView& rv, float margin, cudaStream_t st) 
   return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------- bounded wait
+// The kernels' barrier wait as it is used everywhere (warp_wait: every lane
+// waits, one answer per warp), on a barrier of two arrivals that gets one --
+// or, with ``complete``, both.  A wait that gives up raises the block's abort
+// flag; the block then records DEVERR_TIMEOUT and how long it waited, and
+// returns.  Nothing else is left pending: no copy or MMA was issued.
+__global__ void __launch_bounds__(64) debug_wait_kernel(long long limit_ns, int complete, int64_t* out2) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 2);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    mbar_arrive(&bar);
+    if (complete) mbar_arrive(&bar);
+  }
+  const unsigned long long t0 = globaltimer_ns();
+  const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(&bar, 0, &abort_flag, (unsigned long long)limit_ns));
+  const unsigned long long t1 = globaltimer_ns();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    out2[0] = (ok && !abort_flag) ? 0 : DEVERR_TIMEOUT;
+    out2[1] = (int64_t)(t1 - t0);
+  }
+}
+
+cudaError_t launch_debug_wait(long long limit_ns, bool complete, int64_t* out2, cudaStream_t st) {
+  debug_wait_kernel<<<1, 64, 0, st>>>(limit_ns, complete ? 1 : 0, out2);
+  return cudaGetLastError();
+}
+
 // ---------------------------------------------------------------- debug quantiser
 template <int L>
 __global__ void __launch_bounds__(256) debug_quantize_kernel(const float* __restrict__ x, long long rows,
@@ -425,7 +462,7 @@ __global__ void __launch_bounds__(256) debug_quantize_kernel(const float* __rest
   for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
   amax = row_max<L>(amax, row_group_mask<L>());
   float scale, inv;
-  absmax_scale(amax, scale, inv);
+  row_absmax_scale<L>(amax, scale, inv, row_group_mask<L>());
   *reinterpret_cast<uint4*>(codes + row * D + lane * 16) = quant16(v, inv);
   if (lane == 0) scales[row] = scale;
 }

@@ -39,7 +39,8 @@ EXPORTS = (
     "kvring_set_qk_norm",
     "kvring_reset_positions",
     "kvring_attend", "kvring_destroy", "kvring_status_string", "kvring_last_cuda_error",
-    "kvring_layout", "kvring_debug_state", "kvring_debug_quantize",
+    "kvring_layout", "kvring_debug_state", "kvring_debug_quantize", "kvring_attend_noalloc",
+    "kvring_debug_wait_timeout",
 )
 
 
@@ -94,6 +95,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
                                          ctypes.POINTER(vp), ctypes.POINTER(vp), ctypes.POINTER(i32)]),
         "kvring_debug_state": (ctypes.c_int, [vp, vp, ctypes.POINTER(i32)]),
         "kvring_debug_quantize": (ctypes.c_int, [vp, i64, i32, vp, vp, vp]),
+        "kvring_debug_wait_timeout": (ctypes.c_int, [i64, i32, vp, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -162,7 +164,25 @@ def kvring_write_global(handle, k, v, pos, n: int, stream=None) -> None:
           "kvring_write_global")
 
 
-def kvring_set_qk_norm(handle, gamma_q=None, gamma_k=None, eps: float = 1e-6) -> None:
+def _check_norm_weight(w, numel, device, what):
+    """A norm weight as the kernels read it: contiguous bf16 on the ring's
+    device with exactly H * D values."""
+    if w is None or isinstance(w, int):
+        return
+    if w.dtype != torch.bfloat16 or not w.is_cuda or not w.is_contiguous():
+        raise KVRingError(f"{what}: a contiguous bf16 CUDA tensor is required")
+    if numel is not None and w.numel() != numel:
+        raise KVRingError(f"{what}: {w.numel()} values, the ring needs H * D = {numel} "
+                          "(expand a weight shared by all heads to [H, D])")
+    if device is not None and w.device != torch.device(device):
+        raise KVRingError(f"{what}: on {w.device}, the ring is on {device}")
+
+
+def kvring_set_qk_norm(handle, gamma_q=None, gamma_k=None, eps: float = 1e-6, numel=None, device=None) -> None:
+    """gamma_q / gamma_k: bf16 [H, D] CUDA tensors (or raw device addresses,
+    unchecked); numel / device, when given, are checked against the tensors."""
+    _check_norm_weight(gamma_q, numel, device, "kvring_set_qk_norm gamma_q")
+    _check_norm_weight(gamma_k, numel, device, "kvring_set_qk_norm gamma_k")
     gq = None if gamma_q is None else _ptr(gamma_q)
     gk = None if gamma_k is None else _ptr(gamma_k)
     check(load().kvring_set_qk_norm(handle, gq, gk, float(eps)), "kvring_set_qk_norm")
@@ -190,6 +210,12 @@ def kvring_attend_noalloc(handle, q, q_pos, n_q: int, out, stream=None) -> None:
 
 def kvring_destroy(handle) -> None:
     check(load().kvring_destroy(handle), "kvring_destroy")
+
+
+def kvring_debug_wait_timeout(limit_ns: int, complete: bool, out2, stream=None) -> None:
+    """The library's bounded barrier wait on its own (see kvring.h); out2: int64 [2] CUDA tensor."""
+    check(load().kvring_debug_wait_timeout(int(limit_ns), int(bool(complete)), _ptr(out2), _stream(stream)),
+          "kvring_debug_wait_timeout")
 
 
 def kvring_debug_quantize(x, rows: int, d: int, codes, scales, stream=None) -> None:
@@ -250,8 +276,9 @@ class KVRing:
 
     def set_qk_norm(self, gamma_q=None, gamma_k=None, eps=1e-6):
         """bf16 [H, D] device weights (None: off); the tensors are kept alive here."""
+        kvring_set_qk_norm(self.handle, gamma_q, gamma_k, eps, numel=self.heads * self.head_dim,
+                           device=self.workspace.device)
         self._norm_weights = (gamma_q, gamma_k)
-        kvring_set_qk_norm(self.handle, gamma_q, gamma_k, eps)
 
     def reset_positions(self, d, stream=None):
         kvring_reset_positions(self.handle, d, stream)

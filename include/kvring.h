@@ -77,7 +77,9 @@ enum { KVRING_OUT_BF16 = 0, KVRING_OUT_F32 = 1 };
 
 /*
  * Cache geometry and RoPE layout.
- *   heads      1 .. 128
+ *   heads      1 .. 128 for head_dim 64, 1 .. 64 for head_dim 128
+ *              (heads * head_dim / 16 <= 512: one thread block holds a
+ *              token's heads)
  *   head_dim   64 or 128
  *   n_slots    1 .. 1<<20 ring slots
  *   n_axes     1 .. 3 RoPE axes; axis 0 is the temporal axis (the one the
@@ -182,8 +184,15 @@ int kvring_write_global(kvring* r, const void* k, const void* v, const int32_t* 
  * kvring_attend(_noalloc) normalises Q, in the same kernels.
  *   gamma_q, gamma_k  device bf16 [H][D] weights (16-byte aligned), owned by
  *                     the caller and kept alive while in use; NULL turns
- *                     that norm off (both NULL: no norm, the default)
+ *                     that norm off (both NULL: no norm, the default).  A
+ *                     weight shared by all heads ([D]) must be expanded to
+ *                     [H][D] by the caller: the kernels read H * D values.
  *   eps               > 0 and finite when a weight is given
+ * The K norm belongs to a session: set it before the first write, since a
+ * change later leaves normalised and raw keys side by side in the ring.  On a
+ * calibrated KVRING_SCALES_STATIC ring (whose fixed K scales were taken from
+ * the keys as they were then) a change of the K weights or of eps with K
+ * weights set returns KVRING_ERR_SEQUENCE; the Q norm may change at any time.
  * Per (token, head) row x of D channels: S = sum x_d^2 (bf16 squares summed
  * in fp64, rounded once to fp32), ms = S / D, rstd = 1/sqrt(fl32(ms + eps))
  * correctly rounded, x_d <- bf16(fl32(fl32(x_d * rstd) * gamma_d)); RoPE and
@@ -281,7 +290,9 @@ int kvring_attend(kvring* r, const void* q, const int32_t* q_pos, int32_t n_q, v
  *
  * Set-up: the first call on a device looks up the array's device address
  * (cudaGetSymbolAddress, with that device current, once per device); that
- * first call should come before any stream capture begins.  The ring's
+ * first call should come before any stream capture begins.  The address is
+ * kept for the life of the process: after a cudaDeviceReset (which unloads
+ * the library's device image) this call must not be used again.  The ring's
  * device must be the current device (else KVRING_ERR_INVALID_ARG).
  */
 #define KVRING_NOALLOC_SCRATCH_BYTES (8u << 20)
@@ -313,6 +324,18 @@ int kvring_layout(const kvring* r, void** k_codes, void** v_codes, void** k_scal
  * host<->device read the library offers).
  */
 int kvring_debug_state(const kvring* r, kvring_stream stream, int32_t* out3);
+
+/*
+ * DEBUG: the kernels' bounded barrier wait, on its own.  One block of two
+ * warps waits on a barrier that expects two arrivals; it gets one, or both
+ * when ``complete`` is non-zero.  A wait that has not ended after limit_ns
+ * nanoseconds (1 .. 1e10) gives up the way every wait in the library does: it
+ * raises the block's abort flag, and the block records KVRING_DEVERR_TIMEOUT
+ * and returns.  out2: device int64 [2] = {error bits (0 or
+ * KVRING_DEVERR_TIMEOUT), nanoseconds the wait lasted}, 8-byte aligned.
+ * Asynchronous on ``stream``; the device stays usable afterwards.
+ */
+int kvring_debug_wait_timeout(int64_t limit_ns, int32_t complete, int64_t* out2, kvring_stream stream);
 
 /*
  * The quantiser of ring_kv_write applied to raw fp32 rows, for checking the

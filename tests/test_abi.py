@@ -8,6 +8,7 @@ import os
 import re
 
 import pytest
+import torch
 
 from fp8_ring_kv_gb300 import kvring as K
 
@@ -166,3 +167,13 @@ def test_binding_constants_match_the_header():
     assert len(found) >= 17          # 9 status codes, 3 device error bits, 2 output types, 2 scale modes, 1 size
     for name, value in found.items():
         assert getattr(K, name) == value, name
+
+
+def test_norm_weights_are_checked_in_the_binding():
+    """kvring_set_qk_norm's weights are read as bf16 [H][D] on the device:
+    anything else is refused before the library is called."""
+    from fp8_ring_kv_gb300 import kvring as K
+    with pytest.raises(K.KVRingError, match="bf16"):
+        K.kvring_set_qk_norm(None, torch.zeros(4, dtype=torch.float32), None)
+    with pytest.raises(K.KVRingError, match="bf16"):
+        K.kvring_set_qk_norm(None, None, torch.zeros(4, dtype=torch.bfloat16))   # not on a GPU

@@ -210,6 +210,12 @@ def test_calibration_call_rules():
     assert lib.kvring_calibrate(h, 1.5, None) == K.KVRING_OK
     assert lib.kvring_calibrate(h, 1.5, None) == K.KVRING_ERR_SEQUENCE          # once
     assert lib.kvring_reset_positions(h, 3, None) == K.KVRING_OK
+    # the fixed K scales were taken from un-normalised keys: the K norm may
+    # not change any more, the Q norm may
+    w = torch.ones((sh.heads, sh.head_dim), dtype=torch.bfloat16, device=dev)
+    p = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
+    assert lib.kvring_set_qk_norm(h, None, p(w), 1e-6) == K.KVRING_ERR_SEQUENCE
+    assert lib.kvring_set_qk_norm(h, p(w), None, 1e-6) == K.KVRING_OK
     torch.cuda.synchronize()
     assert ring.debug_state() == (4, 4, 0)
     ring.close()
@@ -273,3 +279,21 @@ def test_fewer_queries_than_the_previous_call():
         compare_attention(out, o.attend(synth.to_f32(q), qpos, heads=heads), f"{n_q} queries")
     assert ring.debug_state()[2] == 0
     ring.close()
+
+
+def test_a_wait_that_runs_out_returns_an_error_status():
+    """The kernels' bounded barrier wait, on a barrier that never completes:
+    after its limit the block records KVRING_DEVERR_TIMEOUT and returns, and
+    the device keeps working (the same wait that completes reports 0)."""
+    K, _ = _lib()
+    out = torch.zeros(2, dtype=torch.int64, device="cuda")
+    limit = 20_000_000                                   # 20 ms
+    K.kvring_debug_wait_timeout(limit, False, out)
+    torch.cuda.synchronize()
+    err, ns = out.tolist()
+    assert err == K.KVRING_DEVERR_TIMEOUT and ns >= limit
+    K.kvring_debug_wait_timeout(limit, True, out)
+    torch.cuda.synchronize()
+    err, ns = out.tolist()
+    assert err == 0 and ns < limit
+    assert int((torch.arange(8, device="cuda") * 2).sum()) == 56

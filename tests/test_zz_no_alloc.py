@@ -56,7 +56,17 @@ def test_noalloc_matches_attend_on_two_calls_in_a_row():
         calls.append((q, pos, want, got))
     # warm the ordinary path and the no-alloc set-up before the memory check
     q, pos, want, got = calls[0]
+    K.kvring_attend(ring.handle, q, pos, q.shape[0], want)
     K.kvring_attend_noalloc(ring.handle, q, pos, q.shape[0], got)
+    torch.cuda.synchronize()
+    # no-alloc calls alone leave the ring's whole workspace as it was (its
+    # query scratch included)
+    before = ring.workspace.clone()
+    for q, pos, want, got in calls:
+        K.kvring_attend_noalloc(ring.handle, q, pos, q.shape[0], got)
+    torch.cuda.synchronize()
+    assert torch.equal(ring.workspace, before), "kvring_attend_noalloc wrote into the ring's workspace"
+    del before
     torch.cuda.synchronize()
     free0, _ = torch.cuda.mem_get_info()
     for i, (q, pos, want, got) in enumerate(calls):

@@ -60,6 +60,8 @@ REROT_BYTES = S * H * (2 * D + 8)                      # K codes + K scale, read
 G = synth.GLOBAL_SLOTS                                 # --layout paper: global slots ahead of the window
 REROT_BYTES_PAPER = (S - G) * H * (2 * D + 8)          # the window keys only
 ATTN_FLOPS = 4 * N * S * D * H                         # QK^T and PV
+# graph replays (of one launch per ring) behind each per-kernel time
+KERNEL_REPS = 50
 # kernels per step: ring_kv_write, delta_rerotate, and the attend call's two
 # (query RoPE + e4m3, then fp8_ring_attn)
 KERNELS_PER_STEP = 4
@@ -257,8 +259,9 @@ def run_gpu(args, rank, world, local_rank):
     secs_max = max_over_ranks(secs, world, dev if world > 1 else "cpu")
     value = aggregate(args.steps, secs_max, world)
 
-    # per-kernel launch time: each kernel alone, back to back over the rings
-    reps = max(1, min(args.steps // R, 400))
+    # per-kernel launch time: each kernel alone, back to back over the rings,
+    # KERNEL_REPS graph replays (R launches each) whatever --steps is
+    reps = KERNEL_REPS
     kern = {}
     for name, fn, work, unit in (
             ("ring_kv_write", lambda r: rings[r].write(inputs[r][0], inputs[r][1], inputs[r][3]), WRITE_BYTES, "GB/s"),
@@ -291,127 +294,290 @@ def run_gpu(args, rank, world, local_rank):
 def run_e2e(args, rings, inputs, dev, world):
     """The same steps through the C-ABI calls with host buffers: every step
     copies its K, V, Q and positions from pinned host memory and copies the
-    attention output back."""
+    attention output back.  The copies run on their own stream into two sets
+    of device buffers, so step i+1's inputs and step i-1's output cross the
+    link while step i computes; events order each copy after the kernels that
+    free or fill its buffer."""
     n = min(args.steps, args.e2e_steps)
     R = len(rings)
     host = []
     for r in range(R):
         k, v, q, pos, out = inputs[r]
-        host.append(tuple(t.cpu().pin_memory() for t in (k, v, q, pos)) + (torch.empty_like(out, device="cpu").pin_memory(),))
-    dbuf = [tuple(torch.empty_like(t) for t in inputs[r][:4]) + (inputs[r][4],) for r in range(R)]
-    st = torch.cuda.current_stream()
+        host.append(tuple(t.cpu().pin_memory() for t in (k, v, q, pos)) +
+                    (torch.empty_like(out, device="cpu").pin_memory(),))
+    dbuf = [tuple(torch.empty_like(t) for t in inputs[0][:5]) for _ in range(2)]
+    comp = torch.cuda.current_stream()
+    copy = torch.cuda.Stream()
+    ev = lambda: torch.cuda.Event()  # noqa: E731
+    h2d_done = [ev(), ev()]
+    freed = [ev(), ev()]      # set b's inputs consumed and its output copied out
+    done = [ev(), ev()]       # set b's kernels done (its output written)
+    for b in range(2):
+        freed[b].record(comp)
 
-    def one(i):
-        r = i % R
-        hk, hv, hq, hp, hout = host[r]
-        dk, dv, dq, dp, dout = dbuf[r]
-        dk.copy_(hk, non_blocking=True)
-        dv.copy_(hv, non_blocking=True)
-        dq.copy_(hq, non_blocking=True)
-        dp.copy_(hp, non_blocking=True)
+    def h2d(i):
+        b, r = i & 1, i % R
+        copy.wait_event(freed[b])
+        with torch.cuda.stream(copy):
+            for dst, src in zip(dbuf[b][:4], host[r][:4]):
+                dst.copy_(src, non_blocking=True)
+        h2d_done[b].record(copy)
+
+    def compute(i):
+        b, r = i & 1, i % R
+        dk, dv, dq, dp, dout = dbuf[b]
+        comp.wait_event(h2d_done[b])
         rings[r].write(dk, dv, dp)
         rings[r].reset_positions(RESET_D)
         rings[r].attend(dq, dp, out=dout)
-        hout.copy_(dout, non_blocking=True)
+        done[b].record(comp)
 
-    for i in range(min(20, n)):
-        one(i)
+    def d2h(i):
+        b, r = i & 1, i % R
+        copy.wait_event(done[b])
+        with torch.cuda.stream(copy):
+            host[r][4].copy_(dbuf[b][4], non_blocking=True)
+        freed[b].record(copy)
+
+    def run(count):
+        h2d(0)
+        for i in range(count):
+            if i + 1 < count:
+                h2d(i + 1)
+            compute(i)
+            d2h(i)
+        comp.wait_stream(copy)
+
+    run(min(20, n))
     torch.cuda.synchronize()
     barrier(world)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(st)
-    for i in range(n):
-        one(i)
-    e1.record(st)
+    e0.record(comp)
+    run(n)
+    e1.record(comp)
     e1.synchronize()
     secs = max_over_ranks(e0.elapsed_time(e1) / 1e3, world, dev if world > 1 else "cpu")
-    h2d = sum(t.numel() * t.element_size() for t in host[0][:4])
-    d2h = host[0][4].numel() * host[0][4].element_size()
+    h2d_b = sum(t.numel() * t.element_size() for t in host[0][:4])
+    d2h_b = host[0][4].numel() * host[0][4].element_size()
     return {"value": round(aggregate(n, secs, world), 2), "unit": "calls/s", "steps": n,
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+            "h2d_bytes_per_step": h2d_b, "d2h_bytes_per_step": d2h_b,
+            "overlap": "copies on a second stream, double-buffered device inputs"}
+
+
+# ---------------------------------------------------------------- the chunk workload
+def run_chunk(dev, reps=3):
+    """The pages' chunk: 60 rings (one per layer) in one allocation, each
+    getting one 757-token write and 4 attends of 757 queries (the denoising
+    passes) per chunk; 8 chunks, the rings reset by 4 x 757 (one batched
+    launch) before chunk 4.  Inputs from the chunk workload's pool of draws
+    (seed 3) through each ring's permutation.  Device ms per chunk, each
+    chunk's launches captured in one graph; also the 60 writes alone, the
+    240 attends alone, and the reset as one batched launch against 60."""
+    from fp8_ring_kv_gb300.kvring import KVRingStack, KVRING_OUT_BF16
+    L = synth.CHUNK_LAYERS
+    shape = synth.Shape(H, D, S, (D,), (-S,), (S + 4 * N,))
+    stack = KVRingStack(L, shape, KVRING_OUT_BF16, max_queries=N)
+    pool = synth.chunk_pool().to(dev)
+    perms = [synth.chunk_layer_blocks(l) for l in range(L)]
+    pre_pos = torch.from_numpy(synth.lin_pos(-S, S)).to(dev)
+    for l, ring in enumerate(stack.rings):
+        p = perms[l]
+        ring.write(torch.cat([pool[int(b)] for b in p[0:8]])[:S], torch.cat([pool[int(b)] for b in p[::-1][0:8]])[:S],
+                   pre_pos)
+    cpos = [torch.from_numpy(synth.lin_pos((c if c < 4 else c - 4) * N, N)).to(dev) for c in range(synth.CHUNKS)]
+    outs = [torch.empty((N, H, D), dtype=torch.bfloat16, device=dev) for _ in range(synth.CHUNK_PASSES)]
+
+    def writes(c):
+        for l, ring in enumerate(stack.rings):
+            p = perms[l]
+            ring.write(pool[int(p[8 + 6 * c])], pool[int(p[9 + 6 * c])], cpos[c])
+
+    def attends(c):
+        for l, ring in enumerate(stack.rings):
+            p = perms[l]
+            for ps in range(synth.CHUNK_PASSES):
+                ring.attend(pool[int(p[10 + 6 * c + ps])], cpos[c], out=outs[ps])
+
+    def chunk(c):
+        if c == 4:
+            stack.reset_positions(4 * N)
+        for l, ring in enumerate(stack.rings):
+            p = perms[l]
+            ring.write(pool[int(p[8 + 6 * c])], pool[int(p[9 + 6 * c])], cpos[c])
+            for ps in range(synth.CHUNK_PASSES):
+                ring.attend(pool[int(p[10 + 6 * c + ps])], cpos[c], out=outs[ps])
+
+    ms = []
+    for c in range(synth.CHUNKS):
+        g = capture(lambda c=c: chunk(c))
+        ms.append(time_graph(g, reps) / reps * 1e3)
+        del g
+    gw = capture(lambda: writes(0))
+    ga = capture(lambda: attends(0))
+    gb = capture(lambda: stack.reset_positions(4 * N))
+    gs = capture(lambda: [r.reset_positions(4 * N) for r in stack.rings])
+    t_w = time_graph(gw, reps) / reps
+    t_a = time_graph(ga, reps) / reps
+    t_b = time_graph(gb, reps) / reps
+    t_s = time_graph(gs, reps) / reps
+    launches = L * (1 + 2 * synth.CHUNK_PASSES)
+    out = {"workload": f"{L} rings x (1 write + {synth.CHUNK_PASSES} attends) per chunk, {synth.CHUNKS} chunks, "
+                       f"batched reset before chunk 4; 24 heads x 128, {S} slots, {N} new tokens",
+           "ms_per_chunk": [round(x, 3) for x in ms], "ms_per_chunk_mean": round(float(np.mean(ms)), 3),
+           "launches_per_chunk": launches, "writes_60_ms": round(t_w * 1e3, 3),
+           "attends_240_ms": round(t_a * 1e3, 3), "attend_call_us_in_chunk": round(t_a / (L * 4) * 1e6, 2),
+           "write_us_in_chunk": round(t_w / L * 1e6, 2),
+           "reset_batched_ms": round(t_b * 1e3, 3), "reset_60_launches_ms": round(t_s * 1e3, 3),
+           "reset_bytes": L * REROT_BYTES,
+           "reset_batched_GBps": round(L * REROT_BYTES / t_b / 1e9, 1)}
+    stack.close()
+    del pool
+    torch.cuda.empty_cache()
+    return out
+
+
+# ---------------------------------------------------------------- the shape sweep
+def run_sweep(dev, reps=5, per_graph=8):
+    """Every shape of the sweep (heads {8,24,48} x head_dim {64,128} x slots
+    {1447, 2894, 5788, 11576}, N = slots x 757 / 5788 rounded, 3-axis RoPE on
+    the latent grid): a ring filled frame by frame, then the write of one
+    frame, the reset by 42 frames and the attend of N queries, each timed
+    alone (graphs of ``per_graph`` launches).  Inputs N(0,1) bf16 drawn on the
+    device (seed 4): timing only, the parity tests cover these shapes."""
+    from fp8_ring_kv_gb300.kvring import KVRing, KVRING_OUT_BF16
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(4)
+    rows = []
+    for (h, d, s) in synth.sweep_shapes():
+        n = synth.sweep_new_tokens(s)
+        F = -(-s // n)
+        shape = synth.sweep(h, d, s).shape
+        ring = KVRing.from_shape(shape, KVRING_OUT_BF16, max_queries=n)
+        rnd = lambda: torch.randn((n, h, d), generator=gen, device=dev).to(torch.bfloat16)  # noqa: E731
+        for t in range(F):
+            ring.write(rnd(), rnd(), torch.from_numpy(synth.sweep_positions(t, n)).to(dev))
+        k, v, q = rnd(), rnd(), rnd()
+        wpos = torch.from_numpy(synth.sweep_positions(F, n)).to(dev)
+        qpos = torch.from_numpy(synth.sweep_positions(F - synth.SWEEP_RESET, n)).to(dev)
+        out = torch.empty((n, h, d), dtype=torch.bfloat16, device=dev)
+        res = {"heads": h, "head_dim": d, "slots": s, "new_tokens": n}
+        work = {"write": n * h * (6 * d + 8) + 4 * n * 3, "rerotate": s * h * (2 * d + 8),
+                "attend": 4 * n * s * d * h}
+        for name, fn in (("write", lambda: ring.write(k, v, wpos)),
+                         ("rerotate", lambda: ring.reset_positions(synth.SWEEP_RESET)),
+                         ("attend", lambda: ring.attend(q, qpos, out=out))):
+            g = capture(lambda fn=fn: [fn() for _ in range(per_graph)])
+            t = time_graph(g, reps) / (reps * per_graph)
+            res[name + "_us"] = round(t * 1e6, 2)
+            if name == "attend":
+                res["attend_TFLOPs"] = round(work[name] / t / 1e12, 1)
+            else:
+                res[name + "_GBps"] = round(work[name] / t / 1e9, 1)
+            del g
+        rows.append(res)
+        ring.close()
+        torch.cuda.empty_cache()
+    return rows
 
 
 # ---------------------------------------------------------------- the oracle (CPU)
 class OracleSample:
-    """The oracle on a sample of the workload, each part timed and scaled to
-    the full step: ``heads`` of the 24 heads; a fraction ``frac`` of the 757
-    new tokens for the write, of the 5,788 cached keys for the reset (a ring
-    of that many slots) and of the 757 query rows for the attention (over all
-    5,788 slots)."""
+    """The oracle on a sample of the workload: heads h0 .. h1-1 of the 24; a
+    fraction ``frac`` of the 757 new tokens for the write, of the 5,788
+    cached keys for the reset (a ring of that many slots) and of the 757 query
+    rows for the attention (over all 5,788 slots).  Each part is timed."""
 
-    def __init__(self, heads=1, frac=1.0):
+    def __init__(self, h0=0, h1=1, frac=1.0):
         from oracle.ring import OracleRing
-        self.heads, self.frac = heads, frac
+        self.h0, self.h1, self.frac = h0, h1, frac
+        heads = h1 - h0
         self.n_w = max(1, int(math.ceil(frac * N)))
         self.s_r = max(1, int(math.ceil(frac * S)))
         self.rows = np.arange(self.n_w)
         pre = list(synth.single().ops)[0]
-        kp, vp = synth.to_f32(pre.k)[:, :heads], synth.to_f32(pre.v)[:, :heads]
+        kp, vp = synth.to_f32(pre.k)[:, h0:h1], synth.to_f32(pre.v)[:, h0:h1]
         g = synth.rng(1, 100)
         ch = synth.outlier_channels(synth.rng(1), H, D)
-        ch = ch[ch < heads * D]                        # those of the sampled heads
-        self.k = synth.to_f32(synth.normal_bf16(g, (N, heads, D), ch))[:self.n_w]
-        self.v = synth.to_f32(synth.normal_bf16(g, (N, heads, D), ch))[:self.n_w]
-        self.q = synth.to_f32(synth.normal_bf16(g, (N, heads, D), ch))
+        self.k = synth.to_f32(synth.normal_bf16(g, (N, H, D), ch))[:self.n_w, h0:h1]
+        self.v = synth.to_f32(synth.normal_bf16(g, (N, H, D), ch))[:self.n_w, h0:h1]
+        self.q = synth.to_f32(synth.normal_bf16(g, (N, H, D), ch))[:, h0:h1]
         self.pos = synth.lin_pos(S, N)
         self.ring = OracleRing(heads, D, S, (D,))
         self.ring.write(kp, vp, pre.pos)
         self.rring = OracleRing(heads, D, self.s_r, (D,))
         self.rring.write(kp[:self.s_r], vp[:self.s_r], pre.pos[:self.s_r])
 
-    def run(self, steps, budget_s=0.0):
-        """Run >= ``steps`` steps (and until ``budget_s`` passes); returns
-        (extrapolated full steps/s, steps run)."""
-        tw = tr = ta = 0.0
-        n = 0
-        t_start = time.time()
-        while n < steps or time.time() - t_start < budget_s:
-            t0 = time.perf_counter()
-            self.ring.write(self.k, self.v, self.pos[:self.n_w])
-            t1 = time.perf_counter()
-            self.rring.reset_positions(RESET_D)
-            t2 = time.perf_counter()
-            self.ring.attend(self.q, self.pos, rows=self.rows)
-            t3 = time.perf_counter()
-            tw, tr, ta = tw + t1 - t0, tr + t2 - t1, ta + t3 - t2
-            n += 1
-        hs = H / self.heads
-        full = (tw * (N / self.n_w) + tr * (S / self.s_r) + ta * (N / self.n_w)) * hs / n
-        return 1.0 / full, n
-
-    def step_seconds(self):
+    def step(self):
+        """One sampled step; returns the seconds of its write, reset and attend."""
         t0 = time.perf_counter()
-        self.run(1)
-        return time.perf_counter() - t0
+        self.ring.write(self.k, self.v, self.pos[:self.n_w])
+        t1 = time.perf_counter()
+        self.rring.reset_positions(RESET_D)
+        t2 = time.perf_counter()
+        self.ring.attend(self.q, self.pos, rows=self.rows)
+        t3 = time.perf_counter()
+        return t1 - t0, t2 - t1, t3 - t2
 
-    def describe(self):
-        return (f"oracle on {self.heads} of {H} heads: write of {self.n_w} of {N} tokens, reset of "
-                f"{self.s_r} of {S} keys, attend of {self.n_w} of {N} query rows over all {S} slots; "
-                f"each part timed and scaled to the full step")
+    def full_step_seconds(self, tw, tr, ta):
+        """The parts' times scaled to the whole rows of a step (these heads)."""
+        return tw * (N / self.n_w) + tr * (S / self.s_r) + ta * (N / self.n_w)
 
 
-def cpu_threads():
-    return os.cpu_count() or 1
+def _oracle_worker(job):
+    """One process of the oracle pool: heads h0 .. h1-1, ``warmup`` untimed
+    steps, then ``steps`` timed ones (at least; more until ``budget_s``
+    passes).  Returns the full-row seconds per timed step."""
+    h0, h1, frac, warmup, steps, budget_s = job
+    np.seterr(all="ignore")
+    smp = OracleSample(h0, h1, frac)
+    for _ in range(warmup):
+        smp.step()
+    out = []
+    t_start = time.time()
+    while len(out) < steps or time.time() - t_start < budget_s:
+        out.append(smp.full_step_seconds(*smp.step()))
+    return out
+
+
+def oracle_pool_rate(procs, frac, warmup, steps, budget_s):
+    """The oracle on ``procs`` host processes at once (spawned, so no GPU
+    state is inherited), the 24 heads dealt out among them.  A step of the
+    whole workload takes as long as the slowest process's share of it; the
+    rate is one over the mean of that over the timed steps.  Returns
+    (steps/s, steps timed, description)."""
+    import multiprocessing as mp
+    procs = max(1, min(procs, H))
+    cuts = [round(i * H / procs) for i in range(procs + 1)]
+    jobs = [(cuts[i], cuts[i + 1], frac, warmup, steps, budget_s) for i in range(procs)]
+    with mp.get_context("spawn").Pool(procs) as pool:
+        per = pool.map(_oracle_worker, jobs)
+    n = min(len(x) for x in per)
+    step_s = [max(x[i] for x in per) for i in range(n)]
+    rate = 1.0 / float(np.mean(step_s))
+    n_w = max(1, int(math.ceil(frac * N)))
+    s_r = max(1, int(math.ceil(frac * S)))
+    desc = (f"oracle (numpy, fp64) in {procs} processes, {max(c1 - c0 for c0, c1 in zip(cuts, cuts[1:]))} of "
+            f"{H} heads each at most; each step samples {n_w} of {N} written tokens, {s_r} of {S} reset keys and "
+            f"{n_w} of {N} query rows (over all {S} slots), and each part's time is scaled to the whole rows "
+            f"(x{N / n_w:.1f}, x{S / s_r:.1f}, x{N / n_w:.1f}): extrapolated; {n} timed steps")
+    return rate, n, desc
 
 
 def run_reference(args, rank, world):
-    """--impl reference: the oracle as it stands on host cores, exactly K
+    """--impl reference: the oracle as it stands on the host cores, exactly K
     timed steps of a bounded sample (after W untimed ones), the sample sized
     so the whole run takes a few minutes."""
     if rank != 0:
         return None
-    budget = 150.0 / max(1, args.steps + args.warmup)      # seconds per step
-    frac = 1.0
-    for _ in range(3):                                     # shrink the sample until a step fits the budget
-        t = OracleSample(heads=1, frac=frac).step_seconds()
-        if t <= budget or frac <= 1e-3:
-            break
-        frac = max(1e-3, frac * budget / t * 0.8)
-    smp = OracleSample(heads=1, frac=frac)
-    smp.run(args.warmup)
+    procs = min(os.cpu_count() or 1, H)
+    per_step = 120.0 / max(1, args.steps + args.warmup)   # seconds per step for the whole run
+    heads_per = -(-H // procs)
+    t1 = OracleSample(0, heads_per, 1.0)
+    t = t1.full_step_seconds(*t1.step())                     # a whole step of one process's heads
+    frac = min(1.0, max(1e-3, per_step / t * 0.8))
     t0 = time.time()
-    rate, n = smp.run(args.steps)
-    return {"value": rate, "desc": smp.describe(), "secs": time.time() - t0, "steps": n}
+    rate, n, desc = oracle_pool_rate(procs, frac, args.warmup, args.steps, 0.0)
+    return {"value": rate, "desc": desc, "secs": time.time() - t0, "steps": n, "cores": procs}
 
 
 # ---------------------------------------------------------------- main
@@ -424,6 +590,8 @@ def main():
     ap.add_argument("--rings", type=int, default=8)
     ap.add_argument("--e2e-steps", type=int, default=2000)
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
+    ap.add_argument("--workload", default="all", choices=["all", "single", "chunk", "sweep"],
+                    help="besides the headline step: the 60-ring chunk and the shape sweep (all), or neither")
     ap.add_argument("--layout", default="ring", choices=["ring", "paper"],
                     help="ring: all 5,788 slots one ring; paper: 1,246 global slots + a 6 x 757 window ring")
     args = ap.parse_args()
@@ -431,6 +599,10 @@ def main():
         raise SystemExit("--warmup must be >= 3")
     rank, world, local_rank = dist_env()
 
+    config = {"workload": WORKLOAD if args.layout == "ring" else WORKLOAD_PAPER,
+              "heads": H, "head_dim": D, "slots": S, "new_tokens": N,
+              "step": "ring_kv_write(757) + delta_rerotate(%d slots) + fp8_ring_attn(757 q)"
+                      % (S if args.layout == "ring" else S - G)}
     if args.impl == "reference":
         np.seterr(all="ignore")
         dist_init(world, "gloo")
@@ -439,13 +611,12 @@ def main():
             line = {"metric": METRIC, "value": round(res["value"], 6), "unit": "calls/s", "n_gpus": args.gpus,
                     "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 / res["value"], 3),
                     "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-                    "data": "synthetic", "impl": "reference",
-                    "config": {"workload": WORKLOAD, "heads": H, "head_dim": D, "slots": S, "new_tokens": N,
-                               "step": "write + rerotate + attend"},
-                    "cpu_baseline": {"value": round(res["value"], 6), "unit": "calls/s", "cores": cpu_threads(),
+                    "data": "synthetic", "impl": "reference", "config": config,
+                    "cpu_baseline": {"value": round(res["value"], 6), "unit": "calls/s", "cores": res["cores"],
                                      "kind": "oracle", "sample": res["desc"]},
                     "e2e": {"value": round(res["value"], 6), "unit": "calls/s", "h2d_bytes_per_step": 0,
-                            "d2h_bytes_per_step": 0}}
+                            "d2h_bytes_per_step": 0},
+                    "wall_s": round(res["secs"], 1)}
             print(json.dumps(line), flush=True)
         if world > 1:
             torch.distributed.destroy_process_group()
@@ -455,13 +626,19 @@ def main():
         raise SystemExit("bench.py needs a CUDA device (the library has no CPU path)")
     dist_init(world, "nccl")
     res = run_gpu(args, rank, world, local_rank)
+    extra = {}
+    if rank == 0 and world == 1 and args.layout == "ring":
+        if args.workload in ("all", "chunk"):
+            extra["chunk"] = run_chunk(torch.device("cuda", local_rank))
+        if args.workload in ("all", "sweep"):
+            extra["sweep"] = run_sweep(torch.device("cuda", local_rank))
     cpu = None
     if rank == 0 and world == 1 and args.cpu_budget > 0 and args.layout == "ring":
-        smp = OracleSample(heads=2)
+        procs = min(os.cpu_count() or 1, H)
         t0 = time.time()
-        rate, n = smp.run(1, budget_s=args.cpu_budget)
-        cpu = {"value": round(rate, 6), "unit": "calls/s", "cores": cpu_threads(), "kind": "oracle",
-               "sample": smp.describe() + f" ({n} sampled steps, {time.time() - t0:.1f} s)"}
+        rate, n, desc = oracle_pool_rate(procs, 1.0, 0, 1, args.cpu_budget)
+        cpu = {"value": round(rate, 6), "unit": "calls/s", "cores": procs, "kind": "oracle",
+               "sample": desc + f" ({time.time() - t0:.1f} s with the pool's start)"}
     if rank == 0:
         att = res["kernels"]["fp8_ring_attn"]
         roof = {"bound": "tensor", "achieved": att["rate"], "peak": round(res["fp8_peak"], 1), "unit": "TFLOP/s",
@@ -472,17 +649,16 @@ def main():
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(res["ms_per_step"], 5),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3/f16/f32",
             "data": "synthetic",
-            "config": {"workload": WORKLOAD if args.layout == "ring" else WORKLOAD_PAPER,
-                       "heads": H, "head_dim": D, "slots": S, "new_tokens": N,
-                       "step": "ring_kv_write(757) + delta_rerotate(%d slots) + fp8_ring_attn(757 q)"
-                               % (S if args.layout == "ring" else S - G),
-                       "rings_cycled": args.rings,
-                       "l2": f"cold by construction: {args.rings} rings x ~50 MB cycled (> 129 MB L2)",
-                       "graphs": "steps replayed from CUDA graphs", "parallelism": f"replicas x{world}"},
+            "config": config,
+            "setup": {"rings_cycled": args.rings,
+                      "l2": f"cold by construction: {args.rings} rings x ~50 MB cycled (> 129 MB L2)",
+                      "graphs": "steps replayed from CUDA graphs", "parallelism": f"replicas x{world}",
+                      "kernel_reps": f"{KERNEL_REPS} graph replays of {args.rings} launches per kernel"},
             "clocks": res["clocks"], "gpu_launches": KERNELS_PER_STEP * args.steps,
             "e2e": res["e2e"], "roofline": roof, "kernels": res["kernels"],
             "cpu_baseline": cpu,
         }
+        line.update(extra)
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()

@@ -198,6 +198,17 @@ int noalloc_scratch(int dev, uint8_t** out) {
   return KVRING_OK;
 }
 
+// cos/sin of the rotation by -d on the temporal axis, fp64 then rounded once
+DeltaTable delta_table(const kvring_config& cfg, int32_t d) {
+  DeltaTable dt{};
+  dt.n_pairs = cfg.axis_dims[0] / 2;
+  for (int j = 0; j < dt.n_pairs; ++j) {
+    const double th = -(double)d * omega(cfg.rope_base, cfg.axis_dims[0], j);
+    dt.cs[j] = make_float2((float)std::cos(th), (float)std::sin(th));
+  }
+  return dt;
+}
+
 }  // namespace
 
 extern "C" {
@@ -324,13 +335,29 @@ int kvring_write_global(kvring* r, const void* k, const void* v, const int32_t* 
 int kvring_reset_positions(kvring* r, int32_t d, kvring_stream stream) {
   if (!r) return KVRING_ERR_INVALID_ARG;
   if (r->cfg.scale_mode == KVRING_SCALES_STATIC && !r->calibrated) return KVRING_ERR_SEQUENCE;
-  DeltaTable dt{};
-  dt.n_pairs = r->cfg.axis_dims[0] / 2;
-  for (int j = 0; j < dt.n_pairs; ++j) {
-    const double th = -(double)d * omega(r->cfg.rope_base, r->cfg.axis_dims[0], j);
-    dt.cs[j] = make_float2((float)std::cos(th), (float)std::sin(th));
+  const cudaError_t e = launch_delta_rerotate(r->rv, delta_table(r->cfg, d), reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? KVRING_OK : cuda_fail(e);
+}
+
+int kvring_reset_positions_batch(kvring* const* rings, int32_t n, int32_t d, kvring_stream stream) {
+  if (!rings || n < 1) return KVRING_ERR_INVALID_ARG;
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  const kvring* r0 = rings[0];
+  if (!r0) return KVRING_ERR_INVALID_ARG;
+  std::vector<const RingView*> rvs((size_t)n);
+  for (int i = 0; i < n; ++i) {
+    const kvring* r = rings[i];
+    if (!r || r->device != dev) return KVRING_ERR_INVALID_ARG;
+    // one rotation table for all: the same head_dim, temporal axis and base
+    if (r->cfg.head_dim != r0->cfg.head_dim || r->cfg.axis_dims[0] != r0->cfg.axis_dims[0] ||
+        r->cfg.rope_base != r0->cfg.rope_base)
+      return KVRING_ERR_INVALID_ARG;
+    if (r->cfg.scale_mode == KVRING_SCALES_STATIC && !r->calibrated) return KVRING_ERR_SEQUENCE;
+    rvs[(size_t)i] = &r->rv;
   }
-  const cudaError_t e = launch_delta_rerotate(r->rv, dt, reinterpret_cast<cudaStream_t>(stream));
+  e = launch_delta_rerotate_batch(rvs.data(), n, delta_table(r0->cfg, d), reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? KVRING_OK : cuda_fail(e);
 }
 

@@ -14,6 +14,21 @@ struct DeltaTable {
   int n_pairs;
 };
 
+// What the rotation of one ring's keys needs (a slice of RingView).
+struct RotRing {
+  uint8_t* k_codes;
+  float* k_scale;
+  int32_t* state;
+  const float* stat;
+  int32_t H, S, S_pad, G, scale_mode;
+};
+
+// Rings rotated by one launch (kernel parameters).
+constexpr int kMaxBatchRings = 32;
+struct RotBatch {
+  RotRing r[kMaxBatchRings];
+};
+
 struct AttnMaps {
   CUtensorMap k_codes;   // [H][S][D] u8, box {D, 128, 1}
   CUtensorMap v_codes;
@@ -43,6 +58,8 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
 cudaError_t launch_ring_kv_write(const RingView& rv, const void* k, const void* v, const int32_t* pos, int n_new,
                                  bool glob, cudaStream_t st);
 cudaError_t launch_delta_rerotate(const RingView& rv, const DeltaTable& dt, cudaStream_t st);
+// the same rotation over n rings of one head_dim, kMaxBatchRings per launch
+cudaError_t launch_delta_rerotate_batch(const RingView* const* rvs, int n, const DeltaTable& dt, cudaStream_t st);
 // per-head fixed scales from the recorded maxima, then every valid row re-quantised with them
 cudaError_t launch_calibrate(const RingView& rv, float margin, cudaStream_t st);
 // one block whose warps wait on a barrier (complete: it is also completed);

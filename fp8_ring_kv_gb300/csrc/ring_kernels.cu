@@ -252,23 +252,20 @@ __global__ void __launch_bounds__(512, 2) q_prep_kernel(RingView rv, const uint4
 // is L lanes of 16 codes; the grid is sized to stay resident and each thread
 // walks rows with a stride of the whole grid, loading its next 16 codes and
 // scale before working on the current ones so that two loads are in flight.
+//
+// The walk over one ring, for thread ``first`` of ``stride`` threads that
+// share the ring (cs_s: the rotation's (cos, sin) per temporal pair, in
+// shared memory: the lanes of a warp read 8 different pairs at once).
 template <int L>
-__global__ void __launch_bounds__(256, 4) delta_rerotate_kernel(RingView rv, DeltaTable dt) {
+__device__ __forceinline__ void rerotate_ring(const RotRing& rv, const float2* cs_s, int n_pairs, int first,
+                                              int stride) {
   constexpr int D = L * 16;
-  // the lanes of a warp read 8 different pairs at once: from shared memory,
-  // not from the parameter space (which would serialise them)
-  __shared__ float2 cs_s[64];
-  if (threadIdx.x < 64) cs_s[threadIdx.x] = dt.cs[threadIdx.x];
-  pdl_wait();
-  pdl_trigger();
-  __syncthreads();
   // rows are walked as (h, s) over the n_win valid window slots, s = slot - G
   const int n_win = rv.state[ST_NVALID] - rv.G;
   if (n_win <= 0) return;
   const bool fixed = rv.scale_mode && rv.state[ST_STATIC];
   const int chunks = rv.H * n_win * L;            // <= 128 heads x 2^20 slots x 8
-  const int stride = gridDim.x * blockDim.x;      // a multiple of 32: rows never split
-  const int lane = threadIdx.x % L;
+  const int lane = threadIdx.x % L;               // stride and first are multiples of 32: rows never split
   // pairs past the temporal axis are left as they are (not rotated by the
   // identity, which would turn a -0 into +0)
   float2 cs[8];
@@ -279,7 +276,7 @@ __global__ void __launch_bounds__(256, 4) delta_rerotate_kernel(RingView rv, Del
   const int row_step = stride / L;
   const int step_h = row_step / n_win;
   const int step_slot = row_step - step_h * n_win;
-  int c = blockIdx.x * blockDim.x + threadIdx.x;
+  int c = first;
   if (c >= chunks) return;   // whole rows
   int h = (c / L) / n_win;
   int slot = c / L - h * n_win;
@@ -313,7 +310,7 @@ __global__ void __launch_bounds__(256, 4) delta_rerotate_kernel(RingView rv, Del
     dequant16_scaled(code, scale, x);
 #pragma unroll
     for (int m = 0; m < 8; ++m)
-      if (lane * 8 + m < dt.n_pairs) rope_pair(x[2 * m], x[2 * m + 1], cs[m].x, cs[m].y);
+      if (lane * 8 + m < n_pairs) rope_pair(x[2 * m], x[2 * m + 1], cs[m].x, cs[m].y);
     if (fixed) {
       // the head's scale is kept; values beyond its range saturate
       *reinterpret_cast<uint4*>(p) = quant16(x, rv.stat[STAT_K_INV * rv.H + h]);
@@ -336,6 +333,30 @@ __global__ void __launch_bounds__(256, 4) delta_rerotate_kernel(RingView rv, Del
     code = code_n;
     scale = scale_n;
   }
+}
+
+template <int L>
+__global__ void __launch_bounds__(256, 4) delta_rerotate_kernel(RotRing rr, DeltaTable dt) {
+  __shared__ float2 cs_s[64];
+  if (threadIdx.x < 64) cs_s[threadIdx.x] = dt.cs[threadIdx.x];
+  pdl_wait();
+  pdl_trigger();
+  __syncthreads();
+  rerotate_ring<L>(rr, cs_s, dt.n_pairs, blockIdx.x * blockDim.x + threadIdx.x, gridDim.x * blockDim.x);
+}
+
+// Several rings in one launch (the rings of every layer at a position reset):
+// blockIdx.y is the ring, the blocks along x share its rows.
+template <int L>
+__global__ void __launch_bounds__(256, 4) delta_rerotate_batch_kernel(const __grid_constant__ RotBatch rb,
+                                                                      DeltaTable dt) {
+  __shared__ float2 cs_s[64];
+  if (threadIdx.x < 64) cs_s[threadIdx.x] = dt.cs[threadIdx.x];
+  pdl_wait();
+  pdl_trigger();
+  __syncthreads();
+  rerotate_ring<L>(rb.r[blockIdx.y], cs_s, dt.n_pairs, blockIdx.x * blockDim.x + threadIdx.x,
+                   gridDim.x * blockDim.x);
 }
 
 // ---------------------------------------------------------------- calibration
@@ -520,6 +541,20 @@ static int rerotate_grid() {
   return blocks;
 }
 
+RotRing rot_ring(const RingView& rv) {
+  RotRing r{};
+  r.k_codes = rv.k_codes;
+  r.k_scale = rv.k_scale;
+  r.state = rv.state;
+  r.stat = rv.stat;
+  r.H = rv.H;
+  r.S = rv.S;
+  r.S_pad = rv.S_pad;
+  r.G = rv.G;
+  r.scale_mode = rv.scale_mode;
+  return r;
+}
+
 cudaError_t launch_delta_rerotate(const RingView& rv, const DeltaTable& dt, cudaStream_t st) {
   const int L = rv.D / 16;
   // enough threads for one pass over a full ring, at most what stays resident
@@ -527,8 +562,35 @@ cudaError_t launch_delta_rerotate(const RingView& rv, const DeltaTable& dt, cuda
   const int resident = L == 4 ? rerotate_grid<4>() : rerotate_grid<8>();
   if (resident <= 0) return cudaErrorInvalidConfiguration;
   const unsigned blocks = (unsigned)(need < resident ? need : resident);
-  if (L == 4) return launch_pdl(delta_rerotate_kernel<4>, dim3(blocks), dim3(256), 0, st, rv, dt);
-  return launch_pdl(delta_rerotate_kernel<8>, dim3(blocks), dim3(256), 0, st, rv, dt);
+  const RotRing rr = rot_ring(rv);
+  if (L == 4) return launch_pdl(delta_rerotate_kernel<4>, dim3(blocks), dim3(256), 0, st, rr, dt);
+  return launch_pdl(delta_rerotate_kernel<8>, dim3(blocks), dim3(256), 0, st, rr, dt);
+}
+
+cudaError_t launch_delta_rerotate_batch(const RingView* const* rvs, int n, const DeltaTable& dt, cudaStream_t st) {
+  if (n < 1) return cudaSuccess;
+  const int L = rvs[0]->D / 16;
+  const int resident = L == 4 ? rerotate_grid<4>() : rerotate_grid<8>();
+  if (resident <= 0) return cudaErrorInvalidConfiguration;
+  for (int i0 = 0; i0 < n; i0 += kMaxBatchRings) {
+    const int m = n - i0 < kMaxBatchRings ? n - i0 : kMaxBatchRings;
+    RotBatch rb{};
+    long long need = 1;
+    for (int i = 0; i < m; ++i) {
+      rb.r[i] = rot_ring(*rvs[i0 + i]);
+      const long long ni = ((long long)rvs[i0 + i]->H * rvs[i0 + i]->S * L + 255) / 256;
+      need = ni > need ? ni : need;
+    }
+    // the resident grid shared among the rings of the launch
+    long long per = resident / m;
+    if (per < 1) per = 1;
+    const unsigned bx = (unsigned)(need < per ? need : per);
+    const cudaError_t e =
+        L == 4 ? launch_pdl(delta_rerotate_batch_kernel<4>, dim3(bx, m), dim3(256), 0, st, rb, dt)
+               : launch_pdl(delta_rerotate_batch_kernel<8>, dim3(bx, m), dim3(256), 0, st, rb, dt);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 cudaError_t launch_debug_quantize(const float* x, long long rows, int d, uint8_t* codes, float* scales,

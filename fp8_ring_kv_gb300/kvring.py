@@ -37,7 +37,7 @@ KVRING_SCALES_STATIC = 1
 EXPORTS = (
     "kvring_workspace_bytes", "kvring_create", "kvring_write", "kvring_write_global", "kvring_calibrate",
     "kvring_set_qk_norm",
-    "kvring_reset_positions",
+    "kvring_reset_positions", "kvring_reset_positions_batch",
     "kvring_attend", "kvring_destroy", "kvring_status_string", "kvring_last_cuda_error",
     "kvring_layout", "kvring_debug_state", "kvring_debug_quantize", "kvring_attend_noalloc",
     "kvring_debug_wait_timeout",
@@ -86,6 +86,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "kvring_calibrate": (ctypes.c_int, [vp, ctypes.c_float, vp]),
         "kvring_set_qk_norm": (ctypes.c_int, [vp, vp, vp, ctypes.c_float]),
         "kvring_reset_positions": (ctypes.c_int, [vp, i32, vp]),
+        "kvring_reset_positions_batch": (ctypes.c_int, [ctypes.POINTER(vp), i32, i32, vp]),
         "kvring_attend": (ctypes.c_int, [vp, vp, vp, i32, vp, vp]),
         "kvring_attend_noalloc": (ctypes.c_int, [vp, vp, vp, i32, vp, vp]),
         "kvring_destroy": (ctypes.c_int, [vp]),
@@ -196,6 +197,12 @@ def kvring_reset_positions(handle, d: int, stream=None) -> None:
     check(load().kvring_reset_positions(handle, int(d), _stream(stream)), "kvring_reset_positions")
 
 
+def kvring_reset_positions_batch(handles, d: int, stream=None) -> None:
+    arr = (ctypes.c_void_p * len(handles))(*[h.value if isinstance(h, ctypes.c_void_p) else h for h in handles])
+    check(load().kvring_reset_positions_batch(arr, len(handles), int(d), _stream(stream)),
+          "kvring_reset_positions_batch")
+
+
 def kvring_attend(handle, q, q_pos, n_q: int, out, stream=None) -> None:
     check(load().kvring_attend(handle, _ptr(q), _ptr(q_pos), int(n_q), _ptr(out), _stream(stream)),
           "kvring_attend")
@@ -232,7 +239,7 @@ class KVRing:
 
     def __init__(self, heads, head_dim, n_slots, axis_dims, pos_min, pos_count, rope_base=10000.0,
                  out_dtype=KVRING_OUT_F32, device="cuda", stream=None, max_queries=None, n_global=0,
-                 scale_mode=KVRING_SCALES_TOKEN):
+                 scale_mode=KVRING_SCALES_TOKEN, workspace=None):
         self.cfg = make_config(heads, head_dim, n_slots, axis_dims, pos_min, pos_count, rope_base, out_dtype,
                                max_queries, n_global, scale_mode)
         nbytes = kvring_workspace_bytes(self.cfg)
@@ -242,7 +249,11 @@ class KVRing:
         self.n_global = int(n_global)
         self.n_axes = len(axis_dims)
         self.out_dtype = torch.float32 if out_dtype == KVRING_OUT_F32 else torch.bfloat16
-        self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        if workspace is None:
+            workspace = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        elif workspace.dtype != torch.uint8 or workspace.numel() < nbytes or workspace.data_ptr() % 256:
+            raise KVRingError("workspace: a uint8 tensor of kvring_workspace_bytes, 256-byte aligned")
+        self.workspace = workspace
         self.handle = kvring_create(self.cfg, self.workspace, stream)
         ptrs = [ctypes.c_void_p() for _ in range(5)]
         s_pad = ctypes.c_int32()
@@ -260,10 +271,12 @@ class KVRing:
         self.state_words = ws[off[4]:off[4] + 16].view(torch.int32)
 
     @classmethod
-    def from_shape(cls, shape, out_dtype=KVRING_OUT_F32, device="cuda", stream=None, max_queries=None):
+    def from_shape(cls, shape, out_dtype=KVRING_OUT_F32, device="cuda", stream=None, max_queries=None,
+                   workspace=None):
         return cls(shape.heads, shape.head_dim, shape.n_slots, shape.axis_dims, shape.pos_min, shape.pos_count,
                    shape.rope_base, out_dtype, device, stream, max_queries, getattr(shape, "n_global", 0),
-                   KVRING_SCALES_STATIC if getattr(shape, "scale_mode", "token") == "static" else KVRING_SCALES_TOKEN)
+                   KVRING_SCALES_STATIC if getattr(shape, "scale_mode", "token") == "static" else KVRING_SCALES_TOKEN,
+                   workspace)
 
     def write(self, k, v, pos, stream=None):
         kvring_write(self.handle, k, v, pos, k.shape[0], stream)
@@ -304,3 +317,32 @@ class KVRing:
             self.close()
         except Exception:
             pass
+
+
+class KVRingStack:
+    """n rings of one shape in ONE device allocation (one slice per ring,
+    each ring with its own state), reset together by one batched launch.
+
+    ``rings[i]`` is a KVRing whose workspace is a view of ``self.workspace``."""
+
+    def __init__(self, n, shape, out_dtype=KVRING_OUT_F32, device="cuda", max_queries=None):
+        if n < 1:
+            raise KVRingError("a stack holds at least one ring")
+        cfg = make_config(shape.heads, shape.head_dim, shape.n_slots, shape.axis_dims, shape.pos_min,
+                          shape.pos_count, shape.rope_base, out_dtype, max_queries, getattr(shape, "n_global", 0),
+                          KVRING_SCALES_STATIC if getattr(shape, "scale_mode", "token") == "static"
+                          else KVRING_SCALES_TOKEN)
+        stride = kvring_workspace_bytes(cfg)
+        if stride == 0:
+            raise KVRingError("invalid kvring configuration")
+        self.stride = stride
+        self.workspace = torch.empty(n * stride, dtype=torch.uint8, device=device)
+        self.rings = [KVRing.from_shape(shape, out_dtype, device, max_queries=max_queries,
+                                        workspace=self.workspace[i * stride:(i + 1) * stride]) for i in range(n)]
+
+    def reset_positions(self, d, stream=None):
+        kvring_reset_positions_batch([r.handle for r in self.rings], d, stream)
+
+    def close(self):
+        for r in self.rings:
+            r.close()

@@ -242,6 +242,23 @@ int kvring_calibrate(kvring* r, float margin, kvring_stream stream);
 int kvring_reset_positions(kvring* r, int32_t d, kvring_stream stream);
 
 /*
+ * The position reset of several rings in one launch (delta_rerotate): the
+ * same as kvring_reset_positions(rings[i], d) for every i, in one kernel
+ * launch per 32 rings instead of one per ring.  Paper App. G: at a reset the
+ * window caches of all the model's blocks are re-rotated; §4.1: the caches of
+ * all layers live in one allocation, each ring a slice of it (a caller that
+ * creates n rings at offsets k * kvring_workspace_bytes(cfg) of one buffer
+ * has that layout; every ring keeps its own state).
+ *   rings  n handles, all on the current device, with the same head_dim,
+ *          axis_dims[0] and rope_base (one rotation table serves them all;
+ *          else KVRING_ERR_INVALID_ARG); heads, n_slots and n_global may
+ *          differ.  A KVRING_SCALES_STATIC ring must be calibrated (else
+ *          KVRING_ERR_SEQUENCE).  Nothing is enqueued if any check fails.
+ *   n      >= 1
+ */
+int kvring_reset_positions_batch(kvring* const* rings, int32_t n, int32_t d, kvring_stream stream);
+
+/*
  * Attention of n_q queries over every valid slot (fp8_ring_attn).  Paper §4.3
  * (queries quantised per call; attention reads the FP8 cache with per-token
  * scales) and App. G (all slots read).

@@ -66,9 +66,10 @@ KERNEL_REPS = 50
 # (query RoPE + e4m3, then fp8_ring_attn)
 KERNELS_PER_STEP = 4
 # DRAM bytes (read + write) of one fp8_ring_attn launch at this workload, from
-# one ncu capture of the kernel as it stands; None while the kernel has
-# changed since the last capture (the row sums now come from the tensor core)
-ATTN_DRAM_BYTES = None
+# one ncu capture of the kernel as it stands (dram__bytes_read.sum 39,156,736
+# + dram__bytes_write.sum 7,424; the capture is summarised in
+# profiles/fp8_ring_attn_single_call.md); None once the kernel changes
+ATTN_DRAM_BYTES = 39_164_160
 
 
 # ---------------------------------------------------------------- distributed helpers

@@ -54,7 +54,8 @@
 //               B operand of PV: V widened, then the u columns (one warp per
 //               sub-partition)
 //   warp 12     TMA producer (the e4m3 query tile, then K, V codes into
-//               NSTAGE stages and their scales into NSC)
+//               NSTAGE stages and, running ahead of them, their scales into
+//               NSC stages)
 //   warp 13     TMEM allocation and MMA issue
 // Every wait is bounded (an error bit and an orderly exit after the limit);
 // the TMA and widening warps, whose work runs ahead of need, park while they
@@ -67,7 +68,7 @@
 namespace kvring_dev {
 
 constexpr int BM = 128;           // query rows per block
-constexpr int BN = 128;           // slots per tile
+constexpr int BN = kAttnKeyTile;  // slots per tile
 constexpr int NSTAGE = 3;         // fp8 K/V stages
 constexpr int NSC = 6;            // scale stages (held until the tile's softmax ends)
 constexpr int ATT_THREADS = 448;
@@ -468,26 +469,35 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
     const int ppos = ((ct & 7) >> 1) * kPermStride + 2 * (ct >> 3) + (ct & 1);
 
     constexpr int CH = D / 16;  // 16-byte e4m3 chunks per slot row
-    for (int u = 0; u < T; ++u) {
-      const int st = u % NSTAGE;
+    // Slot ct of tile u: s_k and w = max(s_v, floor) in the softmax's order,
+    // and u = 2^-c / w as fp16 u_hi + u_lo * 2^-11 (returned, written into
+    // the B operand with the tile's V).  Returns false if the wait gave up.
+    auto prep_scales = [&](int u, __half2& uq) -> bool {
       const int sc = u % NSC;
-      const int b = u & 1;
-      if (!warp_wait(&sc_full[sc], (u / NSC) & 1, abort_flag)) break;
+      if (!warp_wait(&sc_full[sc], (u / NSC) & 1, abort_flag)) return false;
       uint8_t* stage = sm + LY::SC0 + sc * LY::SC_BYTES;
-      // slot ct: s_k and w = max(s_v, floor) in the softmax's order, and
-      // u = 2^-c / w as fp16 u_hi + u_lo * 2^-11
       const float sk = reinterpret_cast<const float*>(stage)[ct];
       const float w = fmaxf(reinterpret_cast<const float*>(stage)[BN + ct], sfloor);
       reinterpret_cast<float*>(stage + 2 * BN * 4)[ppos] = sk;
       reinterpret_cast<float*>(stage + 2 * BN * 4)[4 * kPermStride + ppos] = w;
       const float uv = __fdiv_rn(cscale, w);
       const __half uhi = __float2half_rn(uv);
-      const __half ulo = __float2half_rn((uv - __half2float(uhi)) * 2048.0f);
+      uq = __halves2half2(uhi, __float2half_rn((uv - __half2float(uhi)) * 2048.0f));
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(&sc_ready[sc]);
         mbar_arrive(&sc_empty[sc]);
       }
+      return true;
+    };
+    // The scales run two tiles ahead of the widening, so that the softmax of
+    // tile u + 1 never waits for the widening of tile u.
+    __half2 uq0, uq1, uq2;
+    bool ok = prep_scales(0, uq0) && (T < 2 || prep_scales(1, uq1));
+    for (int u = 0; ok && u < T; ++u) {
+      const int st = u % NSTAGE;
+      const int b = u & 1;
+      if (u + 2 < T && !prep_scales(u + 2, uq2)) break;
       if (!warp_wait(&kv_full[st], (u / NSTAGE) & 1, abort_flag)) break;
       // B operand b is free once PV_{u-2} is done
       if (u >= 2 && !warp_wait(&vh_free[b], ((u - 2) >> 1) & 1, abort_flag)) break;
@@ -495,8 +505,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       uint8_t* vdst = sm + LY::VH0 + b * LY::VH_BYTES;
       {
         uint8_t* ub = vdst + (D / 64) * BN * 128;
-        *reinterpret_cast<__half*>(ub + mn_elem(ct, 0)) = uhi;
-        *reinterpret_cast<__half*>(ub + mn_elem(ct, 1)) = ulo;
+        *reinterpret_cast<__half2*>(ub + mn_elem(ct, 0)) = uq0;
       }
       // eight consecutive threads take the same chunk of eight consecutive
       // slots, so their 16-byte reads and writes fall in distinct bank groups
@@ -529,35 +538,57 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         mbar_arrive(&vh_full[b]);
         mbar_arrive(&kv_empty[st]);
       }
+      uq0 = uq1;
+      uq1 = uq2;
     }
   } else if (warp == WARP_TMA) {
     // ======================================================== TMA producer
+    // One lane issues the query tile, then K, V codes into NSTAGE stages and
+    // their scales into NSC stages, each as soon as its stage is free: it
+    // polls both without blocking (the scales run ahead of the K, V stages)
+    // and sleeps briefly when neither can move.  Bounded like every wait.
     if (lane == 0) {
       mbar_arrive_expect_tx(q_full, BM * D);
       tma_load_3d(sm + LY::Q, &tmQ, q_full, 0, h, qt * BM);
-      int kv_issued = 0, sc_issued = 0;
-      for (int u = 0; u < T; ++u) {
-        const int st = u % NSTAGE;
-        const int sc = u % NSC;
-        if (u >= NSTAGE && !mbar_wait<true>(&kv_empty[st], ((u / NSTAGE) - 1) & 1, abort_flag)) break;
-        mbar_arrive_expect_tx(&kv_full[st], 2 * BN * D);
-        tma_load_3d(sm + LY::K0 + st * BN * D, &tmK, &kv_full[st], 0, u * BN, h);
-        tma_load_3d(sm + LY::V0 + st * BN * D, &tmV, &kv_full[st], 0, u * BN, h);
-        kv_issued = u + 1;
-        if (u >= NSC && !mbar_wait<true>(&sc_empty[sc], ((u / NSC) - 1) & 1, abort_flag)) break;
-        uint8_t* stage = sm + LY::SC0 + sc * LY::SC_BYTES;
-        mbar_arrive_expect_tx(&sc_full[sc], 2 * BN * 4);
-        tma_load_2d(stage, &tmSK, &sc_full[sc], u * BN, h);
-        tma_load_2d(stage + BN * 4, &tmSV, &sc_full[sc], u * BN, h);
-        sc_issued = u + 1;
+      int ukv = 0, usc = 0;
+      unsigned long long t_last = globaltimer_ns();
+      while (ukv < T || usc < T) {
+        bool moved = false;
+        if (ukv < T && (ukv < NSTAGE || mbar_test_wait(&kv_empty[ukv % NSTAGE], ((ukv / NSTAGE) - 1) & 1))) {
+          const int st = ukv % NSTAGE;
+          mbar_arrive_expect_tx(&kv_full[st], 2 * BN * D);
+          tma_load_3d(sm + LY::K0 + st * BN * D, &tmK, &kv_full[st], 0, ukv * BN, h);
+          tma_load_3d(sm + LY::V0 + st * BN * D, &tmV, &kv_full[st], 0, ukv * BN, h);
+          ++ukv;
+          moved = true;
+        }
+        if (usc < T && (usc < NSC || mbar_test_wait(&sc_empty[usc % NSC], ((usc / NSC) - 1) & 1))) {
+          const int sc = usc % NSC;
+          uint8_t* stage = sm + LY::SC0 + sc * LY::SC_BYTES;
+          mbar_arrive_expect_tx(&sc_full[sc], 2 * BN * 4);
+          tma_load_2d(stage, &tmSK, &sc_full[sc], usc * BN, h);
+          tma_load_2d(stage + BN * 4, &tmSV, &sc_full[sc], usc * BN, h);
+          ++usc;
+          moved = true;
+        }
+        if (moved) {
+          t_last = globaltimer_ns();
+        } else {
+          if (*abort_flag) break;
+          if (globaltimer_ns() - t_last > kWaitLimitNs) {
+            *abort_flag = 1;
+            break;
+          }
+          __nanosleep(64);
+        }
       }
       if (*abort_flag) {
         // after an abort: let the copies still in flight land in this
         // block's shared memory before the block exits (time-bounded)
         mbar_wait(q_full, 0, nullptr, 100000000ull);
-        for (int u = max(0, kv_issued - NSTAGE); u < kv_issued; ++u)
+        for (int u = max(0, ukv - NSTAGE); u < ukv; ++u)
           mbar_wait(&kv_full[u % NSTAGE], (u / NSTAGE) & 1, nullptr, 100000000ull);
-        for (int u = max(0, sc_issued - NSC); u < sc_issued; ++u)
+        for (int u = max(0, usc - NSC); u < usc; ++u)
           mbar_wait(&sc_full[u % NSC], (u / NSC) & 1, nullptr, 100000000ull);
       }
     }

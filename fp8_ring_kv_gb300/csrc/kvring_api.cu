@@ -146,7 +146,7 @@ bool encode_maps(kvring* r) {
   {
     const cuuint64_t dims[3] = {D, S, H};
     const cuuint64_t strides[2] = {D, S * D};
-    const cuuint32_t box[3] = {(cuuint32_t)D, 128, 1};
+    const cuuint32_t box[3] = {(cuuint32_t)D, (cuuint32_t)kAttnKeyTile, 1};
     const cuuint32_t es[3] = {1, 1, 1};
     if (enc(&r->maps.k_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, rv.k_codes, dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -160,7 +160,7 @@ bool encode_maps(kvring* r) {
   {
     const cuuint64_t dims[2] = {(cuuint64_t)rv.S_pad, H};
     const cuuint64_t strides[1] = {(cuuint64_t)rv.S_pad * 4};
-    const cuuint32_t box[2] = {128, 1};
+    const cuuint32_t box[2] = {(cuuint32_t)kAttnKeyTile, 1};
     const cuuint32_t es[2] = {1, 1};
     if (enc(&r->maps.k_scale, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, rv.k_scale, dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,

@@ -29,10 +29,14 @@ struct RotBatch {
   RotRing r[kMaxBatchRings];
 };
 
+// Slots per key tile of the attention kernel (the box height of its K, V and
+// scale tensor maps).
+constexpr int kAttnKeyTile = 128;
+
 struct AttnMaps {
-  CUtensorMap k_codes;   // [H][S][D] u8, box {D, 128, 1}
+  CUtensorMap k_codes;   // [H][S][D] u8, box {D, kAttnKeyTile, 1}
   CUtensorMap v_codes;
-  CUtensorMap k_scale;   // [H][S_pad] f32, box {128, 1}
+  CUtensorMap k_scale;   // [H][S_pad] f32, box {kAttnKeyTile, 1}
   CUtensorMap v_scale;
 };
 

@@ -62,6 +62,9 @@ REROT_BYTES_PAPER = (S - G) * H * (2 * D + 8)          # the window keys only
 ATTN_FLOPS = 4 * N * S * D * H                         # QK^T and PV
 # graph replays (of one launch per ring) behind each per-kernel time
 KERNEL_REPS = 50
+# distinct sets of new tokens, queries and positions per ring, cycled by the
+# steps (8 x 757 = 6,056 tokens, more than a ring's 5,788 slots)
+SETS = 8
 # kernels per step: ring_kv_write, delta_rerotate, and the attend call's two
 # (query RoPE + e4m3, then fp8_ring_attn)
 KERNELS_PER_STEP = 4
@@ -154,8 +157,16 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- the GPU arm
-def make_rings(n_rings, dev, layout="ring"):
+def make_rings(n_rings, dev, layout="ring", sets=None):
+    """n_rings rings pre-filled with the single-call workload's 5,788 tokens,
+    and for each ring ``sets`` distinct sets of new tokens, queries and
+    positions drawn with the same recipe.  The steps cycle through the sets,
+    so a ring keeps holding distinct tokens (8 x 757 = 6,056 > 5,788 slots):
+    writing one set over and over would leave the ring full of copies of the
+    same 757 tokens, whose scores barely move from tile to tile, which is not
+    the workload (it made the attention ~12% faster)."""
     from fp8_ring_kv_gb300.kvring import KVRing, KVRING_OUT_BF16
+    sets = SETS if sets is None else sets
     wl = synth.single()
     shape = wl.shape
     if layout == "paper":
@@ -176,13 +187,16 @@ def make_rings(n_rings, dev, layout="ring"):
             ring.write(kp[G:], vp[G:], pp[:S - G])
         else:
             ring.write(kp, vp, pp)
-        g = synth.rng(1, 100 + r)
-        k = synth.normal_bf16(g, (N, H, D), ch).to(dev)
-        v = synth.normal_bf16(g, (N, H, D), ch).to(dev)
-        q = synth.normal_bf16(g, (N, H, D), ch).to(dev)
         out = torch.empty((N, H, D), dtype=torch.bfloat16, device=dev)
+        per = []
+        for t in range(sets):
+            g = synth.rng(1, 100 + r, t)
+            k = synth.normal_bf16(g, (N, H, D), ch).to(dev)
+            v = synth.normal_bf16(g, (N, H, D), ch).to(dev)
+            q = synth.normal_bf16(g, (N, H, D), ch).to(dev)
+            per.append((k, v, q, pos, out))
         rings.append(ring)
-        inputs.append((k, v, q, pos, out))
+        inputs.append(per)
     torch.cuda.synchronize()
     return rings, inputs
 
@@ -209,12 +223,14 @@ def capture(fn):
 
 
 def time_graph(graph, reps):
+    """Seconds for ``reps`` replays of ``graph`` (a list of graphs is cycled)."""
+    graphs = graph if isinstance(graph, (list, tuple)) else [graph]
     st = torch.cuda.current_stream()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     e0.record(st)
-    for _ in range(reps):
-        graph.replay()
+    for i in range(reps):
+        graphs[i % len(graphs)].replay()
     e1.record(st)
     e1.synchronize()
     return e0.elapsed_time(e1) / 1e3
@@ -229,14 +245,25 @@ def run_gpu(args, rank, world, local_rank):
     rings, inputs = make_rings(R, dev, args.layout)
     rerot_bytes = REROT_BYTES_PAPER if args.layout == "paper" else REROT_BYTES
 
-    full = capture(lambda: [step(rings[r], inputs[r]) for r in range(R)])
-    singles = [capture(lambda r=r: step(rings[r], inputs[r])) for r in range(R)]
+    # one graph per token set over all rings, and per (set, ring) for the
+    # steps left over; step i runs on ring i % R with set (i // R) % SETS
+    nsets = len(inputs[0])
+    fulls = [capture(lambda t=t: [step(rings[r], inputs[r][t]) for r in range(R)]) for t in range(nsets)]
+    singles = [[capture(lambda r=r, t=t: step(rings[r], inputs[r][t])) for r in range(R)] for t in range(nsets)]
+    done = [0]
 
     def run_steps(n):
-        for _ in range(n // R):
-            full.replay()
-        for r in range(n % R):
-            singles[r].replay()
+        i = done[0]
+        end = i + n
+        while i < end:
+            t = (i // R) % nsets
+            if i % R == 0 and end - i >= R:
+                fulls[t].replay()
+                i += R
+            else:
+                singles[t][i % R].replay()
+                i += 1
+        done[0] = end
 
     # warm-up, untimed
     run_steps(args.warmup)
@@ -261,15 +288,18 @@ def run_gpu(args, rank, world, local_rank):
     value = aggregate(args.steps, secs_max, world)
 
     # per-kernel launch time: each kernel alone, back to back over the rings,
-    # KERNEL_REPS graph replays (R launches each) whatever --steps is
+    # KERNEL_REPS graph replays (R launches each) whatever --steps is; the
+    # writes and attends cycle through the token sets like the steps
     reps = KERNEL_REPS
     kern = {}
     for name, fn, work, unit in (
-            ("ring_kv_write", lambda r: rings[r].write(inputs[r][0], inputs[r][1], inputs[r][3]), WRITE_BYTES, "GB/s"),
-            ("delta_rerotate", lambda r: rings[r].reset_positions(RESET_D), rerot_bytes, "GB/s"),
-            ("fp8_ring_attn", lambda r: rings[r].attend(inputs[r][2], inputs[r][3], out=inputs[r][4]), ATTN_FLOPS,
-             "TFLOP/s")):
-        g = capture(lambda fn=fn: [fn(r) for r in range(R)])
+            ("ring_kv_write", lambda r, t: rings[r].write(inputs[r][t][0], inputs[r][t][1], inputs[r][t][3]),
+             WRITE_BYTES, "GB/s"),
+            ("delta_rerotate", lambda r, t: rings[r].reset_positions(RESET_D), rerot_bytes, "GB/s"),
+            ("fp8_ring_attn", lambda r, t: rings[r].attend(inputs[r][t][2], inputs[r][t][3], out=inputs[r][t][4]),
+             ATTN_FLOPS, "TFLOP/s")):
+        ts = range(1 if name == "delta_rerotate" else nsets)
+        g = [capture(lambda fn=fn, t=t: [fn(r, t) for r in range(R)]) for t in ts]
         time_graph(g, 2)
         t = time_graph(g, reps) / (reps * R)
         rate = work / t / (1e9 if unit == "GB/s" else 1e12)
@@ -301,12 +331,14 @@ def run_e2e(args, rings, inputs, dev, world):
     free or fill its buffer."""
     n = min(args.steps, args.e2e_steps)
     R = len(rings)
-    host = []
+    nsets = len(inputs[0])
+    host = []   # [ring][set]: K, V, Q, positions, output, in pinned host memory
     for r in range(R):
-        k, v, q, pos, out = inputs[r]
-        host.append(tuple(t.cpu().pin_memory() for t in (k, v, q, pos)) +
-                    (torch.empty_like(out, device="cpu").pin_memory(),))
-    dbuf = [tuple(torch.empty_like(t) for t in inputs[0][:5]) for _ in range(2)]
+        host.append([tuple(t.cpu().pin_memory() for t in inp[:4]) +
+                     (torch.empty_like(inp[4], device="cpu").pin_memory(),) for inp in inputs[r]])
+    dbuf = [tuple(torch.empty_like(t) for t in inputs[0][0][:5]) for _ in range(2)]
+    # step i: ring i % R, set (i // R) % nsets, device buffer set i % 2
+    hs = lambda i: host[i % R][(i // R) % nsets]  # noqa: E731
     comp = torch.cuda.current_stream()
     copy = torch.cuda.Stream()
     ev = lambda: torch.cuda.Event()  # noqa: E731
@@ -317,10 +349,10 @@ def run_e2e(args, rings, inputs, dev, world):
         freed[b].record(comp)
 
     def h2d(i):
-        b, r = i & 1, i % R
+        b = i & 1
         copy.wait_event(freed[b])
         with torch.cuda.stream(copy):
-            for dst, src in zip(dbuf[b][:4], host[r][:4]):
+            for dst, src in zip(dbuf[b][:4], hs(i)[:4]):
                 dst.copy_(src, non_blocking=True)
         h2d_done[b].record(copy)
 
@@ -334,10 +366,10 @@ def run_e2e(args, rings, inputs, dev, world):
         done[b].record(comp)
 
     def d2h(i):
-        b, r = i & 1, i % R
+        b = i & 1
         copy.wait_event(done[b])
         with torch.cuda.stream(copy):
-            host[r][4].copy_(dbuf[b][4], non_blocking=True)
+            hs(i)[4].copy_(dbuf[b][4], non_blocking=True)
         freed[b].record(copy)
 
     def run(count):
@@ -358,8 +390,8 @@ def run_e2e(args, rings, inputs, dev, world):
     e1.record(comp)
     e1.synchronize()
     secs = max_over_ranks(e0.elapsed_time(e1) / 1e3, world, dev if world > 1 else "cpu")
-    h2d_b = sum(t.numel() * t.element_size() for t in host[0][:4])
-    d2h_b = host[0][4].numel() * host[0][4].element_size()
+    h2d_b = sum(t.numel() * t.element_size() for t in host[0][0][:4])
+    d2h_b = host[0][0][4].numel() * host[0][0][4].element_size()
     return {"value": round(aggregate(n, secs, world), 2), "unit": "calls/s", "steps": n,
             "h2d_bytes_per_step": h2d_b, "d2h_bytes_per_step": d2h_b,
             "overlap": "copies on a second stream, double-buffered device inputs"}

@@ -258,34 +258,27 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       rq[sb] = sq > 0.0f ? sq * kRowC : 0x1p-100f;
       m_run[sb] = -INFINITY;
     }
-    // Raise the running maxima of rows a and b to mn0, mn1 at tile j > 0:
-    // O and L hold rows weighted by exp2(-m_run), so once PV_{j-1} (and so
-    // every earlier PV) is done they are brought to exp2(-m_new).  Returns
-    // false if the wait gave up.
-    auto raise_max = [&](int j, float mn0, float mn1) -> bool {
-      if (j > 0) {
-        if (!warp_wait(pv_done, (j - 1) & 1, abort_flag)) return false;
-        tc_fence_after();
-        const float al0 = ex2f(m_run[0] - mn0);
-        const float al1 = ex2f(m_run[1] - mn1);
-        // O's D columns and the 16 of L (the columns past them are unused)
+    // O and L hold rows weighted by exp2(-m_run): when the running maxima of
+    // rows a and b are raised by a tile, the tile's weights use the new
+    // maxima at once, and O and L are brought over (times al0, al1) just
+    // before the tile's P is stored, once PV_{j-1} (and so every earlier PV)
+    // is done -- the wait the P store makes anyway -- and before PV_j adds
+    // the tile.
+    auto rescale_o = [&](float al0, float al1) {
+      // O's D columns and the 16 of L (the columns past them are unused)
 #pragma unroll 1
-        for (int c0 = 0; c0 < D + UN; c0 += 32) {
-          uint32_t o[16];
-          tmem_ld_16x256b_x4(tmem + lanes + TM_O + c0, o);
+      for (int c0 = 0; c0 < D + UN; c0 += 32) {
+        uint32_t o[16];
+        tmem_ld_16x256b_x4(tmem + lanes + TM_O + c0, o);
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            o[4 * k] = __float_as_uint(__uint_as_float(o[4 * k]) * al0);
-            o[4 * k + 1] = __float_as_uint(__uint_as_float(o[4 * k + 1]) * al0);
-            o[4 * k + 2] = __float_as_uint(__uint_as_float(o[4 * k + 2]) * al1);
-            o[4 * k + 3] = __float_as_uint(__uint_as_float(o[4 * k + 3]) * al1);
-          }
-          tmem_st_16x256b_x4(tmem + lanes + TM_O + c0, o);
+        for (int k = 0; k < 4; ++k) {
+          o[4 * k] = __float_as_uint(__uint_as_float(o[4 * k]) * al0);
+          o[4 * k + 1] = __float_as_uint(__uint_as_float(o[4 * k + 1]) * al0);
+          o[4 * k + 2] = __float_as_uint(__uint_as_float(o[4 * k + 2]) * al1);
+          o[4 * k + 3] = __float_as_uint(__uint_as_float(o[4 * k + 3]) * al1);
         }
+        tmem_st_16x256b_x4(tmem + lanes + TM_O + c0, o);
       }
-      m_run[0] = mn0;
-      m_run[1] = mn1;
-      return true;
     };
     bool ok = true;
     for (int j = 0; ok && j < T; ++j) {
@@ -346,7 +339,9 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       // of the tile exceeds it by more than the bound (each thread compares
       // the maximum of its own columns, which exceeds the bound whenever the
       // row's does), or on the first tile: then the rows' maxima are formed
-      // and raised, and O and L rescaled, before the exponentials.
+      // and raised before the exponentials (O and L follow at the P store).
+      float al0 = 1.0f, al1 = 1.0f;
+      bool rescale = false;   // warp-uniform
       if (j == 0 || __any_sync(0xFFFFFFFFu, ma > m_run[0] + kLazyRescale || mb > m_run[1] + kLazyRescale)) {
         ma = fmaxf(ma, __shfl_xor_sync(0xFFFFFFFFu, ma, 1));
         mb = fmaxf(mb, __shfl_xor_sync(0xFFFFFFFFu, mb, 1));
@@ -354,10 +349,13 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         mb = fmaxf(mb, __shfl_xor_sync(0xFFFFFFFFu, mb, 2));
         const float mn0 = (j == 0 || ma > m_run[0] + kLazyRescale) ? fmaxf(m_run[0], ma + kHeadroom) : m_run[0];
         const float mn1 = (j == 0 || mb > m_run[1] + kLazyRescale) ? fmaxf(m_run[1], mb + kHeadroom) : m_run[1];
-        if (!raise_max(j, mn0, mn1)) {
-          ok = false;
-          break;
+        if (j > 0) {
+          al0 = ex2f(m_run[0] - mn0);
+          al1 = ex2f(m_run[1] - mn1);
+          rescale = true;
         }
+        m_run[0] = mn0;
+        m_run[1] = mn1;
       }
       // weights e = exp2(t * rq + c - m) <= 2^(kLazyLog2 + c)
       {
@@ -393,12 +391,13 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
           pk[2 * kk + 1] = cvt_f16x2(pb2.x, pb2.y);
         }
       }
-      // the P buffer was last read by PV_{j-1}
+      // the P buffer was last read by PV_{j-1}, which also finished O and L
       if (j >= 1 && !warp_wait(pv_done, (j - 1) & 1, abort_flag)) {
         ok = false;
         break;
       }
       tc_fence_after();
+      if (rescale) rescale_o(al0, al1);
       tmem_st_16x128b_x16(tmem + lanes + TM_P, pk);
       tc_fence_before();
       __syncwarp();

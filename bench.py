@@ -70,9 +70,9 @@ SETS = 8
 KERNELS_PER_STEP = 4
 # DRAM bytes (read + write) of one fp8_ring_attn launch at this workload, from
 # one ncu capture of the kernel as it stands (dram__bytes_read.sum 39,156,736
-# + dram__bytes_write.sum 7,424; the capture is summarised in
+# + dram__bytes_write.sum 0; the capture is summarised in
 # profiles/fp8_ring_attn_single_call.md); None once the kernel changes
-ATTN_DRAM_BYTES = 39_164_160
+ATTN_DRAM_BYTES = 39_156_736
 
 
 # ---------------------------------------------------------------- distributed helpers

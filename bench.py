@@ -325,18 +325,36 @@ def run_gpu(args, rank, world, local_rank):
 def run_e2e(args, rings, inputs, dev, world):
     """The same steps through the C-ABI calls with host buffers: every step
     copies its K, V, Q and positions from pinned host memory and copies the
-    attention output back.  The copies run on their own stream into two sets
-    of device buffers, so step i+1's inputs and step i-1's output cross the
-    link while step i computes; events order each copy after the kernels that
-    free or fill its buffer."""
+    attention output back.  A step's inputs lie back to back in one pinned
+    buffer and cross in one copy; the library is called on views of the
+    device copy.  The copies run on their own stream into two sets of device
+    buffers, so step i+1's inputs and step i-1's output cross the link while
+    step i computes; events order each copy after the kernels that free or
+    fill its buffer."""
     n = min(args.steps, args.e2e_steps)
     R = len(rings)
     nsets = len(inputs[0])
-    host = []   # [ring][set]: K, V, Q, positions, output, in pinned host memory
+    k0, v0, q0, p0, o0 = inputs[0][0]
+    parts = (k0, v0, q0, p0)
+    sizes = [t.numel() * t.element_size() for t in parts]
+    offs = [sum(sizes[:i]) for i in range(len(sizes))]   # 4.65 MB each: every part 256-byte aligned
+
+    def views(buf):
+        return tuple(buf[o:o + n].view(t.dtype).view(t.shape) for o, n, t in zip(offs, sizes, parts))
+
+    host = []   # [ring][set]: (K, V, Q, positions back to back, output), in pinned host memory
     for r in range(R):
-        host.append([tuple(t.cpu().pin_memory() for t in inp[:4]) +
-                     (torch.empty_like(inp[4], device="cpu").pin_memory(),) for inp in inputs[r]])
-    dbuf = [tuple(torch.empty_like(t) for t in inputs[0][0][:5]) for _ in range(2)]
+        per = []
+        for inp in inputs[r]:
+            hb = torch.empty(sum(sizes), dtype=torch.uint8).pin_memory()
+            for dst, src in zip(views(hb), inp[:4]):
+                dst.copy_(src)
+            per.append((hb, torch.empty_like(inp[4], device="cpu").pin_memory()))
+        host.append(per)
+    dbuf = []
+    for _ in range(2):
+        db = torch.empty(sum(sizes), dtype=torch.uint8, device=dev)
+        dbuf.append((db,) + views(db) + (torch.empty_like(o0),))
     # step i: ring i % R, set (i // R) % nsets, device buffer set i % 2
     hs = lambda i: host[i % R][(i // R) % nsets]  # noqa: E731
     comp = torch.cuda.current_stream()
@@ -352,13 +370,12 @@ def run_e2e(args, rings, inputs, dev, world):
         b = i & 1
         copy.wait_event(freed[b])
         with torch.cuda.stream(copy):
-            for dst, src in zip(dbuf[b][:4], hs(i)[:4]):
-                dst.copy_(src, non_blocking=True)
+            dbuf[b][0].copy_(hs(i)[0], non_blocking=True)
         h2d_done[b].record(copy)
 
     def compute(i):
         b, r = i & 1, i % R
-        dk, dv, dq, dp, dout = dbuf[b]
+        _, dk, dv, dq, dp, dout = dbuf[b]
         comp.wait_event(h2d_done[b])
         rings[r].write(dk, dv, dp)
         rings[r].reset_positions(RESET_D)
@@ -369,7 +386,7 @@ def run_e2e(args, rings, inputs, dev, world):
         b = i & 1
         copy.wait_event(done[b])
         with torch.cuda.stream(copy):
-            hs(i)[4].copy_(dbuf[b][4], non_blocking=True)
+            hs(i)[1].copy_(dbuf[b][5], non_blocking=True)
         freed[b].record(copy)
 
     def run(count):
@@ -390,11 +407,11 @@ def run_e2e(args, rings, inputs, dev, world):
     e1.record(comp)
     e1.synchronize()
     secs = max_over_ranks(e0.elapsed_time(e1) / 1e3, world, dev if world > 1 else "cpu")
-    h2d_b = sum(t.numel() * t.element_size() for t in host[0][0][:4])
-    d2h_b = host[0][0][4].numel() * host[0][0][4].element_size()
+    h2d_b = host[0][0][0].numel()
+    d2h_b = host[0][0][1].numel() * host[0][0][1].element_size()
     return {"value": round(aggregate(n, secs, world), 2), "unit": "calls/s", "steps": n,
             "h2d_bytes_per_step": h2d_b, "d2h_bytes_per_step": d2h_b,
-            "overlap": "copies on a second stream, double-buffered device inputs"}
+            "overlap": "one input copy and one output copy per step on a second stream, double-buffered device inputs"}
 
 
 # ---------------------------------------------------------------- the chunk workload

@@ -492,8 +492,10 @@ def run_sweep(dev, reps=5, per_graph=8):
     {1447, 2894, 5788, 11576}, N = slots x 757 / 5788 rounded, 3-axis RoPE on
     the latent grid): a ring filled frame by frame, then the write of one
     frame, the reset by 42 frames and the attend of N queries, each timed
-    alone (graphs of ``per_graph`` launches).  Inputs N(0,1) bf16 drawn on the
-    device (seed 4): timing only, the parity tests cover these shapes."""
+    alone (graphs of ``per_graph`` launches; the writes of a graph each take
+    their own frame, so the ring keeps distinct tokens: per_graph = 8 frames
+    of N fill any ring of the sweep).  Inputs N(0,1) bf16 drawn on the device (seed 4): timing
+    only, the parity tests cover these shapes."""
     from fp8_ring_kv_gb300.kvring import KVRing, KVRING_OUT_BF16
     gen = torch.Generator(device=dev)
     gen.manual_seed(4)
@@ -506,17 +508,18 @@ def run_sweep(dev, reps=5, per_graph=8):
         rnd = lambda: torch.randn((n, h, d), generator=gen, device=dev).to(torch.bfloat16)  # noqa: E731
         for t in range(F):
             ring.write(rnd(), rnd(), torch.from_numpy(synth.sweep_positions(t, n)).to(dev))
-        k, v, q = rnd(), rnd(), rnd()
+        kv = [(rnd(), rnd()) for _ in range(per_graph)]
+        q = rnd()
         wpos = torch.from_numpy(synth.sweep_positions(F, n)).to(dev)
         qpos = torch.from_numpy(synth.sweep_positions(F - synth.SWEEP_RESET, n)).to(dev)
         out = torch.empty((n, h, d), dtype=torch.bfloat16, device=dev)
         res = {"heads": h, "head_dim": d, "slots": s, "new_tokens": n}
         work = {"write": n * h * (6 * d + 8) + 4 * n * 3, "rerotate": s * h * (2 * d + 8),
                 "attend": 4 * n * s * d * h}
-        for name, fn in (("write", lambda: ring.write(k, v, wpos)),
-                         ("rerotate", lambda: ring.reset_positions(synth.SWEEP_RESET)),
-                         ("attend", lambda: ring.attend(q, qpos, out=out))):
-            g = capture(lambda fn=fn: [fn() for _ in range(per_graph)])
+        for name, fn in (("write", lambda i: ring.write(kv[i][0], kv[i][1], wpos)),
+                         ("rerotate", lambda i: ring.reset_positions(synth.SWEEP_RESET)),
+                         ("attend", lambda i: ring.attend(q, qpos, out=out))):
+            g = capture(lambda fn=fn: [fn(i) for i in range(per_graph)])
             t = time_graph(g, reps) / (reps * per_graph)
             res[name + "_us"] = round(t * 1e6, 2)
             if name == "attend":

@@ -33,14 +33,15 @@
 // 2^-c), keeps a zero or near-zero V row's weight in L; it changes that row's
 // own (near-zero) values by at most 448 * floor.
 //
-// Pipeline.  TMEM holds two 128-column S buffers, one 64-column P buffer
-// (fp16 pairs) and the O accumulator with the row sums L in 16 columns after
-// it.  Each softmax warp loads its S lanes into registers and at once releases
-// the buffer, and QK_{j+2} refills it while the softmax works on tile j + 1;
-// the softmax of tile j stores its P once PV_{j-1} has read the previous one.
-// The MMA sequence is QK_0, QK_1, then per tile j: QK_{j+2} (once every
-// softmax warp has read S_j) and PV_j (once P_j and the fp16 V_j are in).  No
-// MMA writes TMEM that another MMA may still read.  A tile whose maximum passes
+// Pipeline.  TMEM holds two 128-column S buffers and the O accumulator with
+// the row sums L in 16 columns after it.  The softmax of tile j loads S_j
+// from buffer j % 2 into registers and stores P_j (fp16 pairs) over the first
+// 64 columns of the same buffer; the MMA sequence is QK_0, QK_1, then per
+// tile j: PV_j (once P_j and the fp16 V_j are in) and, once PV_j is done
+// reading P_j, QK_{j+2} into that buffer.  So the softmax of tile j + 1 runs
+// while PV_j and QK_{j+2} execute, and it never waits for a PV unless the
+// tile raises a row maximum (O and L are then rescaled once PV_j is done).
+// No MMA writes TMEM that another MMA may still read.  A tile whose maximum passes
 // the bound is found before its exponentials (the row maxima are voted on
 // first), so no weight can overflow.  TMEM lane quarter q can only be read by
 // the warps of SM sub-partition q, so the softmax of rows 32q .. 32q+31 runs on
@@ -79,9 +80,8 @@ constexpr int CONV_THREADS = 32 * CONV_WARPS;
 constexpr int WARP_TMA = SOFT_WARPS + CONV_WARPS;
 constexpr int WARP_MMA = WARP_TMA + 1;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t TM_S = 0;      // S buffer b: fp32 [128 lanes][128] at columns 128 b
-constexpr uint32_t TM_P = 256;    // P: fp16 pairs [128 lanes][64]
-constexpr uint32_t TM_O = 320;    // O: fp32 [128 lanes][D], then L: columns D (hi) and D + 1 (lo) of 16
+constexpr uint32_t TM_S = 0;      // buffer b at columns 128 b: S fp32 [128 lanes][128], then P over it: fp16 pairs [128][64]
+constexpr uint32_t TM_O = 256;    // O: fp32 [128 lanes][D], then L: columns D (hi) and D + 1 (lo) of 16
 constexpr int UN = 16;            // columns of PV's N given to the row sums
 // The softmax thread (c4 = lane % 4) of the 16x256b shape reads columns
 // 8k + 2 c4 + e (k < 16, e < 2) of a tile; their scales are stored at
@@ -117,7 +117,7 @@ struct AttnLayout {
   static constexpr int VH0 = V0 + NSTAGE * BN * D;       // 2 x VH_BYTES
   static constexpr int SC0 = VH0 + 2 * VH_BYTES;         // NSC x {s_k [BN], s_v [BN], perm s_k, perm w}
   static constexpr int BAR = SC0 + NSC * SC_BYTES;
-  static constexpr int NBAR = 2 * NSTAGE + 3 * NSC + 2 * 2 + 2 + 2 * 2 + 2;
+  static constexpr int NBAR = 2 * NSTAGE + 3 * NSC + 2 * 2 + 1 + 2 * 2 + 2;
   static constexpr int MISC = BAR + NBAR * 8;
   static constexpr int BYTES = MISC + 64;
   static constexpr int ALLOC = BYTES + 1024;             // slack for 1024-byte alignment
@@ -163,14 +163,13 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
   uint64_t* sc_full = kv_empty + NSTAGE;        // [NSC] raw scales landed
   uint64_t* sc_ready = sc_full + NSC;           // [NSC] scales in the softmax's order (and w) written
   uint64_t* sc_empty = sc_ready + NSC;          // [NSC] the tile's softmax and u columns are done
-  uint64_t* s_full = sc_empty + NSC;            // [2] QK done into S buffer b
-  uint64_t* s_free = s_full + 2;                // [2] every softmax warp has read S buffer b
-  uint64_t* p_full = s_free + 2;                // P stored (once per tile)
-  uint64_t* pv_done = p_full + 1;               // PV (and row sums) done (once per tile)
+  uint64_t* s_full = sc_empty + NSC;            // [2] QK done into buffer b
+  uint64_t* p_full = s_full + 2;                // [2] every softmax warp has stored its P over buffer b
+  uint64_t* pv_done = p_full + 2;               // PV (and row sums) done (once per tile)
   uint64_t* vh_full = pv_done + 1;              // [2] fp16 B operand b written
   uint64_t* vh_free = vh_full + 2;              // [2] PV of the tile in B operand b done
   uint64_t* q_full = vh_free + 2;               // query tile landed
-  uint64_t* mma_drain = q_full + 1;             // every issued MMA done (before TMEM is released)
+  uint64_t* mma_drain = q_full + 1;             // every issued MMA done (O final; before TMEM is released)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + LY::MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + LY::MISC + 4);
 
@@ -191,11 +190,10 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       mbar_init(&sc_ready[i], CONV_WARPS);
       mbar_init(&sc_empty[i], SOFT_WARPS + CONV_WARPS);   // the softmax, the widening warps
     }
-    mbar_init(p_full, SOFT_WARPS);
     mbar_init(pv_done, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&s_free[i], SOFT_WARPS);
+      mbar_init(&p_full[i], SOFT_WARPS);
       mbar_init(&vh_full[i], CONV_WARPS);
       mbar_init(&vh_free[i], 1);
     }
@@ -261,9 +259,8 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
     // O and L hold rows weighted by exp2(-m_run): when the running maxima of
     // rows a and b are raised by a tile, the tile's weights use the new
     // maxima at once, and O and L are brought over (times al0, al1) just
-    // before the tile's P is stored, once PV_{j-1} (and so every earlier PV)
-    // is done -- the wait the P store makes anyway -- and before PV_j adds
-    // the tile.
+    // before the tile's P is stored: once PV_{j-1} (and so every earlier PV)
+    // is done, and before PV_j adds the tile.
     auto rescale_o = [&](float al0, float al1) {
       // O's D columns and the 16 of L (the columns past them are unused)
 #pragma unroll 1
@@ -291,10 +288,6 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       tc_fence_after();
       uint32_t xr[64];
       tmem_ld_16x256b_x16(tmem + lanes + TM_S + 128 * b, xr);
-      // S is in registers: the buffer is free for QK_{j+2}
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s_free[b]);
       float* x = reinterpret_cast<float*>(xr);
       const uint8_t* stage = sm + LY::SC0 + sc * LY::SC_BYTES;
       const float4* psk = reinterpret_cast<const float4*>(stage + 2 * BN * 4) + c4 * (kPermStride / 4);
@@ -391,18 +384,22 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
           pk[2 * kk + 1] = cvt_f16x2(pb2.x, pb2.y);
         }
       }
-      // the P buffer was last read by PV_{j-1}, which also finished O and L
-      if (j >= 1 && !warp_wait(pv_done, (j - 1) & 1, abort_flag)) {
-        ok = false;
-        break;
+      if (rescale) {
+        // PV_{j-2} is done (QK_j, which wrote S_j, was issued after it), so
+        // the phase of pv_done that completes next, or last, is PV_{j-1}'s
+        if (!warp_wait(pv_done, (j - 1) & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        rescale_o(al0, al1);
       }
-      tc_fence_after();
-      if (rescale) rescale_o(al0, al1);
-      tmem_st_16x128b_x16(tmem + lanes + TM_P, pk);
+      // P_j over the S_j just read (this warp's lanes, columns 0 .. 63)
+      tmem_st_16x128b_x16(tmem + lanes + TM_S + 128 * b, pk);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(p_full);
+        mbar_arrive(&p_full[b]);
         mbar_arrive(&sc_empty[sc]);
       }
     }
@@ -411,7 +408,10 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
     // per thread (thread t <-> lane 32*quarter + t), and each writes half of
     // the output columns.
     const int r = 32 * quarter + lane;
-    ok = ok && warp_wait(pv_done, (T - 1) & 1, abort_flag);
+    // O and L are final once every MMA is done (after an abort the drain
+    // completes too, but the output is then not written)
+    ok = ok && warp_wait(mma_drain, 0, abort_flag);
+    ok = ok && __shfl_sync(0xFFFFFFFFu, *abort_flag == 0, 0);
     if (ok) {
       tc_fence_after();
       uint32_t lr[2];
@@ -593,9 +593,9 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
     }
   } else {
     // ======================================================== MMA issue
-    // QK_0, QK_1, then per tile j: QK_{j+2} into S buffer j % 2 once every
-    // softmax warp has read S_j (and K_{j+2} is in), and PV_j (with the row
-    // sums) once P_j and the fp16 B operand are in.
+    // QK_0, QK_1, then per tile j: PV_j (with the row sums) once P_j and the
+    // fp16 B operand are in, and QK_{j+2} into buffer j % 2 once PV_j has
+    // read P_j there (and K_{j+2} is in).
     if (lane == 0) {
       constexpr uint32_t idesc_qk = make_idesc(0, 0, 0, 0, BM, BN);        // e4m3 x e4m3, both K-major
       constexpr uint32_t idesc_pv = make_idesc(0, 0, 0, 1, BM, D + UN);    // f16 x f16, B MN-major
@@ -618,22 +618,23 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
       if (T > 1) ok = ok && issue_qk(1);
       for (int j = 0; ok && j < T; ++j) {
         const int b = j & 1;
-        if (j + 2 < T) {
-          if (!mbar_wait(&s_free[b], (j >> 1) & 1, abort_flag)) break;
-          tc_fence_after();
-          if (!issue_qk(j + 2)) break;
-        }
-        if (!mbar_wait(p_full, j & 1, abort_flag) || !mbar_wait(&vh_full[b], (j >> 1) & 1, abort_flag)) break;
+        if (!mbar_wait(&p_full[b], (j >> 1) & 1, abort_flag) || !mbar_wait(&vh_full[b], (j >> 1) & 1, abort_flag)) break;
         tc_fence_after();
         const uint32_t va = smem_u32(sm + LY::VH0 + b * LY::VH_BYTES);
         // 16 slots per MMA: A = 8 columns of P (fp16 pairs), B = 16 rows of
         // [V | u] (2 KB down the 128-byte rows of each column block)
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
-          mma_f16_ts(tmem + TM_O, tmem + TM_P + kk * 8, make_sdesc_sw128(va + kk * 16 * 128, BN * 128, 1024),
+          mma_f16_ts(tmem + TM_O, tmem + TM_S + 128 * b + kk * 8, make_sdesc_sw128(va + kk * 16 * 128, BN * 128, 1024),
                      idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
         mma_commit(pv_done);
         mma_commit(&vh_free[b]);
+        if (j + 2 < T) {
+          // QK_{j+2} overwrites the P that PV_j reads
+          if (!mbar_wait(pv_done, j & 1, abort_flag)) break;
+          tc_fence_after();
+          if (!issue_qk(j + 2)) break;
+        }
       }
       // every MMA issued so far is done before the block releases TMEM
       mma_commit(mma_drain);

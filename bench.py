@@ -69,10 +69,10 @@ SETS = 8
 # (query RoPE + e4m3, then fp8_ring_attn)
 KERNELS_PER_STEP = 4
 # DRAM bytes (read + write) of one fp8_ring_attn launch at this workload, from
-# one ncu capture of the kernel as it stands (dram__bytes_read.sum 39,156,736
+# one ncu capture of the kernel as it stands (dram__bytes_read.sum 39,155,968
 # + dram__bytes_write.sum 0; the capture is summarised in
 # profiles/fp8_ring_attn_single_call.md); None once the kernel changes
-ATTN_DRAM_BYTES = 39_156_736
+ATTN_DRAM_BYTES = 39_155_968
 
 
 # ---------------------------------------------------------------- distributed helpers
@@ -327,10 +327,13 @@ def run_e2e(args, rings, inputs, dev, world):
     copies its K, V, Q and positions from pinned host memory and copies the
     attention output back.  A step's inputs lie back to back in one pinned
     buffer and cross in one copy; the library is called on views of the
-    device copy.  The copies run on their own stream into two sets of device
-    buffers, so step i+1's inputs and step i-1's output cross the link while
-    step i computes; events order each copy after the kernels that free or
-    fill its buffer."""
+    device copy.  Inputs and outputs cross on two streams of their own (the
+    two directions of the link at once), through three sets of device
+    buffers: step i+1's inputs and step i-1's output move while step i
+    computes.  Events order each copy after the kernels that free or fill
+    its buffer: an input copy waits for the kernels that read the set's
+    previous inputs, a step's kernels for the copy out of the set's previous
+    output."""
     n = min(args.steps, args.e2e_steps)
     R = len(rings)
     nsets = len(inputs[0])
@@ -351,43 +354,46 @@ def run_e2e(args, rings, inputs, dev, world):
                 dst.copy_(src)
             per.append((hb, torch.empty_like(inp[4], device="cpu").pin_memory()))
         host.append(per)
+    NB = 3
     dbuf = []
-    for _ in range(2):
+    for _ in range(NB):
         db = torch.empty(sum(sizes), dtype=torch.uint8, device=dev)
         dbuf.append((db,) + views(db) + (torch.empty_like(o0),))
-    # step i: ring i % R, set (i // R) % nsets, device buffer set i % 2
+    # step i: ring i % R, set (i // R) % nsets, device buffer set i % NB
     hs = lambda i: host[i % R][(i // R) % nsets]  # noqa: E731
     comp = torch.cuda.current_stream()
-    copy = torch.cuda.Stream()
+    copy_in, copy_out = torch.cuda.Stream(), torch.cuda.Stream()
     ev = lambda: torch.cuda.Event()  # noqa: E731
-    h2d_done = [ev(), ev()]
-    freed = [ev(), ev()]      # set b's inputs consumed and its output copied out
-    done = [ev(), ev()]       # set b's kernels done (its output written)
-    for b in range(2):
-        freed[b].record(comp)
+    h2d_done = [ev() for _ in range(NB)]   # set b's inputs landed
+    d2h_done = [ev() for _ in range(NB)]   # set b's output copied out
+    done = [ev() for _ in range(NB)]       # set b's kernels done (inputs read, output written)
+    for b in range(NB):
+        done[b].record(comp)
+        d2h_done[b].record(comp)
 
     def h2d(i):
-        b = i & 1
-        copy.wait_event(freed[b])
-        with torch.cuda.stream(copy):
+        b = i % NB
+        copy_in.wait_event(done[b])
+        with torch.cuda.stream(copy_in):
             dbuf[b][0].copy_(hs(i)[0], non_blocking=True)
-        h2d_done[b].record(copy)
+        h2d_done[b].record(copy_in)
 
     def compute(i):
-        b, r = i & 1, i % R
+        b, r = i % NB, i % R
         _, dk, dv, dq, dp, dout = dbuf[b]
         comp.wait_event(h2d_done[b])
+        comp.wait_event(d2h_done[b])
         rings[r].write(dk, dv, dp)
         rings[r].reset_positions(RESET_D)
         rings[r].attend(dq, dp, out=dout)
         done[b].record(comp)
 
     def d2h(i):
-        b = i & 1
-        copy.wait_event(done[b])
-        with torch.cuda.stream(copy):
+        b = i % NB
+        copy_out.wait_event(done[b])
+        with torch.cuda.stream(copy_out):
             hs(i)[1].copy_(dbuf[b][5], non_blocking=True)
-        freed[b].record(copy)
+        d2h_done[b].record(copy_out)
 
     def run(count):
         h2d(0)
@@ -396,7 +402,8 @@ def run_e2e(args, rings, inputs, dev, world):
                 h2d(i + 1)
             compute(i)
             d2h(i)
-        comp.wait_stream(copy)
+        comp.wait_stream(copy_in)
+        comp.wait_stream(copy_out)
 
     run(min(20, n))
     torch.cuda.synchronize()
@@ -411,7 +418,7 @@ def run_e2e(args, rings, inputs, dev, world):
     d2h_b = host[0][0][1].numel() * host[0][0][1].element_size()
     return {"value": round(aggregate(n, secs, world), 2), "unit": "calls/s", "steps": n,
             "h2d_bytes_per_step": h2d_b, "d2h_bytes_per_step": d2h_b,
-            "overlap": "one input copy and one output copy per step on a second stream, double-buffered device inputs"}
+            "overlap": "one input copy and one output copy per step, on two copy streams, three device buffer sets"}
 
 
 # ---------------------------------------------------------------- the chunk workload

@@ -59,8 +59,8 @@
 //               NSC stages)
 //   warp 13     TMEM allocation and MMA issue
 // Every wait is bounded (an error bit and an orderly exit after the limit);
-// the TMA and widening warps, whose work runs ahead of need, park while they
-// wait so that their polling leaves issue slots to the softmax warps.
+// the TMA lane, whose loads run ahead of need, sleeps briefly whenever no
+// stage can move, so that its polling leaves issue slots to the softmax.
 #include <cfloat>
 
 #include "common.cuh"

@@ -64,22 +64,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// The same, but parked until the phase completes or about kSuspendHintNs
-// pass: for waiters off the critical path, so that their polling leaves the
-// issue slots to the warps that share their SM sub-partition.
-constexpr uint32_t kSuspendHintNs = 20000;   // 20 us
-__device__ __forceinline__ bool mbar_try_wait_parked(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendHintNs)
-      : "memory");
-  return ok != 0;
-}
-
 // Non-blocking test of the phase (never suspends the thread): for a waiter
 // that polls several barriers in turn.
 __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
@@ -98,17 +82,14 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
 // stops waiting) once ``*abort`` becomes non-zero or ``limit_ns`` passes; in
 // the latter case it raises ``*abort`` itself so every other role of the
 // block stops waiting too.  ``abort`` may be null (a wait that only the time
-// limit ends, for draining copies after an abort).  kParked: see
-// mbar_try_wait_parked.
-template <bool kParked = false>
+// limit ends, for draining copies after an abort).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
                                           unsigned long long limit_ns = kWaitLimitNs) {
-  auto probe = [&]() { return kParked ? mbar_try_wait_parked(bar, parity) : mbar_try_wait(bar, parity); };
-  if (probe()) return true;
+  if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer_ns();
   uint32_t spins = 0;
   while (true) {
-    if (probe()) return true;
+    if (mbar_try_wait(bar, parity)) return true;
     if ((++spins & 7u) == 0) {
       if (abort && *abort) return false;
       if (globaltimer_ns() - t0 > limit_ns) {
@@ -119,35 +100,11 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
-// The same as mbar_wait, polling with the non-blocking test (the thread is
-// never suspended): for waits on the critical path, where a suspended
-// thread's late wake-up would cost more than the issue slots of the poll.
-__device__ __forceinline__ bool mbar_wait_spin(uint64_t* bar, uint32_t parity, volatile int* abort) {
-  if (mbar_test_wait(bar, parity)) return true;
-  const unsigned long long t0 = globaltimer_ns();
-  uint32_t spins = 0;
-  while (true) {
-    if (mbar_test_wait(bar, parity)) return true;
-    if ((++spins & 15u) == 0) {
-      if (*abort) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
-        *abort = 1;
-        return false;
-      }
-    }
-  }
-}
-
-__device__ __forceinline__ bool warp_wait_spin(uint64_t* bar, uint32_t parity, volatile int* abort) {
-  return __all_sync(0xFFFFFFFFu, mbar_wait_spin(bar, parity, abort));
-}
-
 // mbar_wait by every lane of a warp, with one answer for all of them (a lane
 // that timed out while another saw the phase complete must not leave the warp
 // divergent at a later warp-collective instruction).
-template <bool kParked = false>
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
-  return __all_sync(0xFFFFFFFFu, mbar_wait<kParked>(bar, parity, abort));
+  return __all_sync(0xFFFFFFFFu, mbar_wait(bar, parity, abort));
 }
 
 // ---------------------------------------------------------------- dependent launch

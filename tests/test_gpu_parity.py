@@ -61,6 +61,16 @@ def test_sweep(heads, head_dim, n_slots):
     assert rep.attend_checked == 1
 
 
+@pytest.mark.parametrize("heads,head_dim", [(64, 128), (128, 64)])
+def test_largest_head_counts(heads, head_dim):
+    """The largest head counts the library accepts (2 * heads * head_dim / 16 =
+    1024: one 512-thread block per token in the write and query kernels),
+    through the sweep workload on a 1,447-slot ring that wraps: every cache
+    bit for bit, the attention of all heads within the tolerance."""
+    rep = replay(synth.sweep(heads, head_dim, 1447), cache_every=1)
+    assert rep.writes == 9 and rep.resets == 1 and rep.attend_checked == 1
+
+
 def test_global_slots_tiny_3axis():
     """Global slots written once, a 3-frame window ring that wraps twice, a
     reset that must leave the globals alone; everything compared after every

@@ -71,6 +71,34 @@ def test_largest_head_counts(heads, head_dim):
     assert rep.writes == 9 and rep.resets == 1 and rep.attend_checked == 1
 
 
+def _tile_exact():
+    """A 1,024-slot ring (eight 128-slot key tiles) whose valid count is a
+    whole number of tiles at every attend (896, then 1,024, then full after
+    wrapping writes), queried by exactly one and two 128-query tiles: the
+    kernels' paths with no partial key or query tile.  Seed 12."""
+    H, D, S = 8, 128, 1024
+    shape = synth.Shape(H, D, S, (D,), (0,), (4096,))
+
+    def ops():
+        g = synth.rng(12)
+        yield synth.Write(synth.normal_bf16(g, (896, H, D)), synth.normal_bf16(g, (896, H, D)), synth.lin_pos(0, 896))
+        yield synth.Attend(synth.normal_bf16(g, (128, H, D)), synth.lin_pos(768, 128), tag="n896_q128")
+        for t, n_q in ((0, 128), (1, 256)):
+            start = 896 + 128 * t
+            yield synth.Write(synth.normal_bf16(g, (128, H, D)), synth.normal_bf16(g, (128, H, D)),
+                              synth.lin_pos(start, 128))
+            yield synth.Attend(synth.normal_bf16(g, (n_q, H, D)), synth.lin_pos(start + 128 - n_q, n_q),
+                               tag=f"w{t}_q{n_q}")
+        yield synth.Reset(512)
+        yield synth.Attend(synth.normal_bf16(g, (256, H, D)), synth.lin_pos(400, 256), tag="after_reset")
+    return synth.Workload("tile_exact", shape, 1, ops())
+
+
+def test_whole_tiles_of_slots_and_queries():
+    rep = replay(_tile_exact(), cache_every=1)
+    assert rep.writes == 3 and rep.resets == 1 and rep.attend_checked == 4
+
+
 def test_global_slots_tiny_3axis():
     """Global slots written once, a 3-frame window ring that wraps twice, a
     reset that must leave the globals alone; everything compared after every

@@ -662,7 +662,8 @@ def main():
     config = {"workload": WORKLOAD if args.layout == "ring" else WORKLOAD_PAPER,
               "heads": H, "head_dim": D, "slots": S, "new_tokens": N,
               "step": "ring_kv_write(757) + delta_rerotate(%d slots) + fp8_ring_attn(757 q)"
-                      % (S if args.layout == "ring" else S - G)}
+                      % (S if args.layout == "ring" else S - G),
+              "l2": f"cold by construction: {args.rings} rings x ~50 MB cycled (> 129 MB L2)"}
     if args.impl == "reference":
         np.seterr(all="ignore")
         dist_init(world, "gloo")
@@ -711,7 +712,6 @@ def main():
             "data": "synthetic",
             "config": config,
             "setup": {"rings_cycled": args.rings,
-                      "l2": f"cold by construction: {args.rings} rings x ~50 MB cycled (> 129 MB L2)",
                       "graphs": "steps replayed from CUDA graphs", "parallelism": f"replicas x{world}",
                       "kernel_reps": f"{KERNEL_REPS} graph replays of {args.rings} launches per kernel"},
             "clocks": res["clocks"], "gpu_launches": KERNELS_PER_STEP * args.steps,

@@ -165,6 +165,20 @@ def kvring_write_global(handle, k, v, pos, n: int, stream=None) -> None:
           "kvring_write_global")
 
 
+def _check_rows(t, n, trailing, dtype, device, what):
+    """A tensor the kernels read or write as n rows of ``trailing`` elements:
+    at least n rows (the kernels touch the first n only), of ``dtype``,
+    contiguous, on the ring's ``device``."""
+    if tuple(t.shape[1:]) != tuple(trailing) or t.shape[0] < n:
+        raise KVRingError(f"{what}: shape {tuple(t.shape)}; the call reads [{n}, {', '.join(map(str, trailing))}]")
+    if t.dtype != dtype:
+        raise KVRingError(f"{what}: {t.dtype}; the kernels read {dtype}")
+    if not t.is_contiguous():
+        raise KVRingError(f"{what}: not contiguous")
+    if t.device != torch.device(device):
+        raise KVRingError(f"{what}: on {t.device}, the ring is on {device}")
+
+
 def _check_norm_weight(w, numel, device, what):
     """A norm weight as the kernels read it: contiguous bf16 on the ring's
     device with exactly H * D values."""
@@ -278,11 +292,24 @@ class KVRing:
                    KVRING_SCALES_STATIC if getattr(shape, "scale_mode", "token") == "static" else KVRING_SCALES_TOKEN,
                    workspace)
 
+    def _check_tokens(self, what, n, pairs):
+        """bf16 [n, H, D] token tensors and int32 [n, n_axes] positions on the ring's device."""
+        dev = self.workspace.device
+        for name, t in pairs:
+            if name.endswith("pos"):
+                _check_rows(t, n, (self.n_axes,), torch.int32, dev, f"{what} {name}")
+            else:
+                _check_rows(t, n, (self.heads, self.head_dim), torch.bfloat16, dev, f"{what} {name}")
+
     def write(self, k, v, pos, stream=None):
-        kvring_write(self.handle, k, v, pos, k.shape[0], stream)
+        n = k.shape[0]
+        self._check_tokens("write", n, (("k", k), ("v", v), ("pos", pos)))
+        kvring_write(self.handle, k, v, pos, n, stream)
 
     def write_global(self, k, v, pos, stream=None):
-        kvring_write_global(self.handle, k, v, pos, k.shape[0], stream)
+        n = k.shape[0]
+        self._check_tokens("write_global", n, (("k", k), ("v", v), ("pos", pos)))
+        kvring_write_global(self.handle, k, v, pos, n, stream)
 
     def calibrate(self, margin=1.5, stream=None):
         kvring_calibrate(self.handle, margin, stream)
@@ -297,9 +324,12 @@ class KVRing:
         kvring_reset_positions(self.handle, d, stream)
 
     def attend(self, q, q_pos, out=None, stream=None):
+        n = q.shape[0]
+        self._check_tokens("attend", n, (("q", q), ("q_pos", q_pos)))
         if out is None:
             out = torch.empty(q.shape, dtype=self.out_dtype, device=q.device)
-        kvring_attend(self.handle, q, q_pos, q.shape[0], out, stream)
+        _check_rows(out, n, (self.heads, self.head_dim), self.out_dtype, self.workspace.device, "attend out")
+        kvring_attend(self.handle, q, q_pos, n, out, stream)
         return out
 
     def debug_state(self, stream=None):

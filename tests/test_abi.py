@@ -177,3 +177,22 @@ def test_norm_weights_are_checked_in_the_binding():
         K.kvring_set_qk_norm(None, torch.zeros(4, dtype=torch.float32), None)
     with pytest.raises(K.KVRingError, match="bf16"):
         K.kvring_set_qk_norm(None, None, torch.zeros(4, dtype=torch.bfloat16))   # not on a GPU
+
+
+def test_ring_wrapper_checks_tensor_arguments():
+    """The KVRing wrapper's checks of the token, position and output tensors
+    (shape, dtype, contiguity, device) before any call reaches the library."""
+    from fp8_ring_kv_gb300.kvring import KVRingError, _check_rows
+    cpu = torch.device("cpu")
+    k = torch.zeros((5, 3, 64), dtype=torch.bfloat16)
+    _check_rows(k, 5, (3, 64), torch.bfloat16, cpu, "k")              # as the kernels read it
+    _check_rows(k, 4, (3, 64), torch.bfloat16, cpu, "k")              # extra rows are not read
+    for t, n, msg in ((k, 6, "shape"), (k[:, :2], 5, "shape"), (k.float(), 5, "float32"),
+                      (torch.zeros((64, 3, 5), dtype=torch.bfloat16).transpose(0, 2), 5, "contiguous")):
+        with pytest.raises(KVRingError, match=msg):
+            _check_rows(t, n, (3, 64), torch.bfloat16, cpu, "k")
+    with pytest.raises(KVRingError, match="the ring is on"):
+        _check_rows(k, 5, (3, 64), torch.bfloat16, torch.device("cuda", 0), "k")
+    pos = torch.zeros((5, 3), dtype=torch.int64)
+    with pytest.raises(KVRingError, match="int64"):
+        _check_rows(pos, 5, (3,), torch.int32, cpu, "pos")

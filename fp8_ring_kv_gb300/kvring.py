@@ -169,13 +169,14 @@ def _check_rows(t, n, trailing, dtype, device, what):
     """A tensor the kernels read or write as n rows of ``trailing`` elements:
     at least n rows (the kernels touch the first n only), of ``dtype``,
     contiguous, on the ring's ``device``."""
-    if tuple(t.shape[1:]) != tuple(trailing) or t.shape[0] < n:
-        raise KVRingError(f"{what}: shape {tuple(t.shape)}; the call reads [{n}, {', '.join(map(str, trailing))}]")
+    shape = t.shape
+    if shape[1:] != trailing or shape[0] < n:
+        raise KVRingError(f"{what}: shape {tuple(shape)}; the call reads [{n}, {', '.join(map(str, trailing))}]")
     if t.dtype != dtype:
         raise KVRingError(f"{what}: {t.dtype}; the kernels read {dtype}")
     if not t.is_contiguous():
         raise KVRingError(f"{what}: not contiguous")
-    if t.device != torch.device(device):
+    if t.device != device:
         raise KVRingError(f"{what}: on {t.device}, the ring is on {device}")
 
 
@@ -297,9 +298,9 @@ class KVRing:
         dev = self.workspace.device
         for name, t in pairs:
             if name.endswith("pos"):
-                _check_rows(t, n, (self.n_axes,), torch.int32, dev, f"{what} {name}")
+                _check_rows(t, n, (self.n_axes,), torch.int32, dev, name)
             else:
-                _check_rows(t, n, (self.heads, self.head_dim), torch.bfloat16, dev, f"{what} {name}")
+                _check_rows(t, n, (self.heads, self.head_dim), torch.bfloat16, dev, name)
 
     def write(self, k, v, pos, stream=None):
         n = k.shape[0]
@@ -328,7 +329,7 @@ class KVRing:
         self._check_tokens("attend", n, (("q", q), ("q_pos", q_pos)))
         if out is None:
             out = torch.empty(q.shape, dtype=self.out_dtype, device=q.device)
-        _check_rows(out, n, (self.heads, self.head_dim), self.out_dtype, self.workspace.device, "attend out")
+        _check_rows(out, n, (self.heads, self.head_dim), self.out_dtype, self.workspace.device, "out")
         kvring_attend(self.handle, q, q_pos, n, out, stream)
         return out
 

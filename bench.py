@@ -334,6 +334,7 @@ def run_e2e(args, rings, inputs, dev, world):
     its buffer: an input copy waits for the kernels that read the set's
     previous inputs, a step's kernels for the copy out of the set's previous
     output."""
+    from fp8_ring_kv_gb300 import kvring as K
     n = min(args.steps, args.e2e_steps)
     R = len(rings)
     nsets = len(inputs[0])
@@ -378,14 +379,17 @@ def run_e2e(args, rings, inputs, dev, world):
             dbuf[b][0].copy_(hs(i)[0], non_blocking=True)
         h2d_done[b].record(copy_in)
 
+    n_tok = k0.shape[0]
+
     def compute(i):
         b, r = i % NB, i % R
         _, dk, dv, dq, dp, dout = dbuf[b]
         comp.wait_event(h2d_done[b])
         comp.wait_event(d2h_done[b])
-        rings[r].write(dk, dv, dp)
-        rings[r].reset_positions(RESET_D)
-        rings[r].attend(dq, dp, out=dout)
+        h = rings[r].handle
+        K.kvring_write(h, dk, dv, dp, n_tok, comp)
+        K.kvring_reset_positions(h, RESET_D, comp)
+        K.kvring_attend(h, dq, dp, n_tok, dout, comp)
         done[b].record(comp)
 
     def d2h(i):

@@ -87,6 +87,14 @@ def test_workspace_bytes_rejects_invalid(lib, field, value):
     assert K.kvring_workspace_bytes(paper_config(**{field: value})) == 0
 
 
+def test_head_count_limit(lib):
+    """2 * heads * head_dim / 16 <= 1024 (one block of at most 512 threads per
+    token in the write and query kernels): 64 heads at D = 128, 128 at D = 64."""
+    for heads, dim, ok in ((64, 128, True), (65, 128, False), (128, 64, True), (129, 64, False)):
+        c = K.make_config(heads, dim, 512, (dim,), (0,), (1024,))
+        assert (K.kvring_workspace_bytes(c) > 0) == ok, (heads, dim)
+
+
 def test_workspace_bytes_rejects_bad_axes(lib):
     c = paper_config()
     c.axis_dims[0] = 30                       # axes no longer sum to head_dim
